@@ -1,0 +1,430 @@
+#!/usr/bin/env python3
+"""Benchmark: CP prefill causal TFLOP/s on one GB300 (both ring schedules).
+
+One step = one layer's CP prefill with Pass-KV followed by the same layer with
+Pass-Q, on the 128K-token workload (batch 1, 16 q heads, 1 kv head, head_dim
+128, 16 CP chunks of 8192, causal, bf16).  value = causal-effective FLOPs of
+the step / device time.  Inputs are resident in HBM before the timed region;
+Q and O (512 MiB each) are larger than L2, so no L2 flush is inserted.
+
+Also reported: ms per layer of each schedule at 128K and at 1M tokens, the
+roofline of the dominant kernel (live CUDA-event timing of every launch), the
+end-to-end number through the host-buffer entry point, and the fp64 CPU
+oracle timed on a bounded sample of rows (baseline only).
+
+--impl reference times that oracle as the reference arm (CPU, rank 0 only).
+Multi-GPU: "replicas only" -- each rank runs the whole step on its own GPU
+with no data-path collective (weak scaling); value sums all ranks' FLOPs over
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CP prefill causal TFLOP/s & % of GB300 BF16 peak; ms/layer at 128K and 1M tokens"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+# DRAM bytes (read + write) per launch of the tensor-core attention kernel
+# from one ncu capture, and the kernel source it was taken from.  Set to None
+# until a capture of the current source exists.
+TRAFFIC_RECORD = None  # {"sha": "...", "bytes_per_flop": float, "capture": "..."}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        out = {}
+        for key in ("bf16_tflops", "bf16_tflops_sustained", "hbm_gbs"):
+            val = d.get(key)
+            if isinstance(val, dict):
+                val = val.get("value")
+            if val is not None:
+                out[key] = float(val)
+        if "bf16_tflops" in out:
+            return out, "measured"
+    except (OSError, ValueError):
+        pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sha():
+    p = os.path.join(ROOT, "context_ring_attention_cpattn_gb300", "csrc", "attn_tc.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_median": statistics.median(power), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- oracle legs
+def oracle_sample(w, n_rows, seed=7):
+    """Time the fp64 oracle on n_rows seeded query rows of workload w (host cores)."""
+    import numpy as np
+
+    import oracle
+    from context_ring_attention_cpattn_gb300.workloads import make_qkv
+
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(w.sq, size=n_rows, replace=False))
+    q, k, v = make_qkv(w, device="cpu")
+    qs = q[:, rows].float().numpy()
+    kh, vh = k.float().numpy(), v.float().numpy()
+    threads = oracle.default_threads()
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.attention(qs, kh, vh, q_pos=w.q_base + rows, causal=w.causal, threads=threads)
+    dt = time.perf_counter() - t0
+    pos = w.q_base + rows
+    vis = np.minimum(pos + 1, w.skv).clip(min=0).sum() if w.causal else n_rows * w.skv
+    flops = 4.0 * w.head_dim * w.hq * w.batch * float(vis)
+    return flops, dt, threads, rows
+
+
+def run_reference(args, w):
+    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return 0
+    n_rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample(w, n_rows)
+    tot_f, tot_t, threads = 0.0, 0.0, 1
+    for s in range(args.steps):
+        f, dt, threads, _ = oracle_sample(w, n_rows, seed=100 + s)
+        tot_f += f
+        tot_t += dt
+    value = tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "hq": w.hq, "hkv": w.hkv,
+                   "head_dim": w.head_dim, "seq_len": w.sq, "n_chunks": w.n_chunks},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n_rows} seeded query rows x {w.hq} heads of the {w.name} "
+                                   f"workload per step, full causal key range"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+def time_modes(B, w, q, k, v, outs, wss, steps, warmup, world, profile_cap=0):
+    """Warm up, then time `steps` steps of (Pass-KV, Pass-Q).  Returns the
+    elapsed ms (max over ranks), per-mode ms lists and profile records."""
+    import torch
+
+    modes = (B.PASS_KV, B.PASS_Q)
+
+    def one(mode):
+        o, lse = outs[mode]
+        B.prefill(q, k, v, w.n_chunks, mode, q_base=w.q_base, causal=w.causal, out=o, lse=lse,
+                  workspace=wss[mode])
+
+    for _ in range(warmup):
+        for m in modes:
+            one(m)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(modes) + 1)]
+          for _ in range(steps)]
+    if profile_cap:
+        B.profile_begin(profile_cap)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for s in range(steps):
+        ev[s][0].record(stream)
+        for x, m in enumerate(modes):
+            one(m)
+            ev[s][x + 1].record(stream)
+    end.record(stream)
+    end.synchronize()
+    recs = B.profile_end(profile_cap) if profile_cap else []
+    torch.cuda.synchronize()
+    barrier(world)
+    elapsed = start.elapsed_time(end)
+    per_mode = {m: [ev[s][x].elapsed_time(ev[s][x + 1]) for s in range(steps)]
+                for x, m in enumerate(modes)}
+    return max_over_ranks(elapsed, world), per_mode, recs
+
+
+def make_buffers(B, w, q, k):
+    import torch
+
+    outs, wss = {}, {}
+    for mode in (B.PASS_KV, B.PASS_Q):
+        outs[mode] = (torch.empty_like(q),
+                      torch.empty((w.batch, w.hq, w.sq), dtype=torch.float32, device=q.device))
+        n = B.workspace_size(q, k, w.n_chunks, mode, w.q_base, w.causal)
+        wss[mode] = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    return outs, wss
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="128k")
+    ap.add_argument("--skip-1m", action="store_true", help="do not time the 1M-token layer")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=96, help="oracle rows for cpu_baseline")
+    ap.add_argument("--ref-rows", type=int, default=16, help="oracle rows per reference step")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: warmup raised to 3 (timing rule)", file=sys.stderr)
+        args.warmup = 3
+
+    from context_ring_attention_cpattn_gb300.workloads import WORKLOADS
+
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+
+    world, rank, local = dist_setup()
+    from context_ring_attention_cpattn_gb300 import binding as B
+    from context_ring_attention_cpattn_gb300 import build as pkg_build
+    from context_ring_attention_cpattn_gb300.workloads import make_qkv
+
+    if rank == 0 or world == 1:
+        pkg_build.build()
+    barrier(world)
+    B.lib()
+
+    q, k, v = make_qkv(w, device="cuda")
+    outs, wss = make_buffers(B, w, q, k)
+    flops_layer = w.causal_flops()
+    flops_step = 2 * flops_layer
+    launches_per_step = 0
+    for mode in (B.PASS_KV, B.PASS_Q):
+        plan = B.prefill_plan(w.sq, w.skv, w.n_chunks, mode, w.q_base, w.causal)
+        launches_per_step += len({e[0] for e in plan}) + 1
+    cap = (launches_per_step + 4) * args.steps
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    elapsed, per_mode, recs = time_modes(B, w, q, k, v, outs, wss, args.steps, args.warmup, world,
+                                         profile_cap=cap)
+    clk = clocks.stop()
+    ms_step = elapsed / args.steps
+    value = world * flops_step * args.steps / (elapsed * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    tc = [r for r in recs if r[0] == "attn_tc"]
+    tc_ms = sum(r[1] for r in tc)
+    tc_flops = sum(r[2] for r in tc)
+    achieved = tc_flops / (tc_ms * 1e-3) / 1e12 if tc_ms > 0 else None
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    traffic = None
+    if TRAFFIC_RECORD and TRAFFIC_RECORD.get("sha") == kernel_sha() and tc:
+        traffic = TRAFFIC_RECORD["bytes_per_flop"] * tc_flops / len(tc)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+                "kernel": "attn_tc_kernel (tcgen05 partial attention)",
+                "peak_source": f"{peak_src} bf16 dense, sustained",
+                "launches_timed": len(tc), "avg_launch_ms": tc_ms / len(tc) if tc else None,
+                "share_of_step": tc_ms / elapsed if elapsed else None}
+
+    ms_layer = {"pass_kv": statistics.median(per_mode[B.PASS_KV]),
+                "pass_q": statistics.median(per_mode[B.PASS_Q])}
+    cfg = {"workload": w.name, "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim,
+           "seq_len": w.sq, "n_chunks": w.n_chunks, "causal": w.causal,
+           "step": "Pass-KV prefill + Pass-Q prefill of one layer",
+           "flops_per_layer": flops_layer, "ms_per_layer": ms_layer,
+           "tflops_per_schedule": {k_: flops_layer / (v_ * 1e-3) / 1e12 for k_, v_ in ms_layer.items()},
+           "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+           "peak_bf16_tflops": peaks["bf16_tflops"], "peak_source": peak_src,
+           "l2": "inputs larger than L2: Q and O are 512 MiB each (K/V 32 MiB each stay L2-resident, as on a CP rank)",
+           "parallelism": f"replicas x{world}"}
+
+    # ---- 1M-token layer (ms/layer only)
+    if not args.skip_1m and w.name != "1m":
+        del outs, wss
+        torch.cuda.empty_cache()
+        w1 = WORKLOADS["1m"]
+        q1, k1, v1 = make_qkv(w1, device="cuda")
+        outs1, wss1 = make_buffers(B, w1, q1, k1)
+        steps1 = max(1, args.steps // 5)
+        _, pm1, _ = time_modes(B, w1, q1, k1, v1, outs1, wss1, steps1, 1, world)
+        ms1 = {"pass_kv": statistics.median(pm1[B.PASS_KV]), "pass_q": statistics.median(pm1[B.PASS_Q])}
+        f1 = w1.causal_flops()
+        cfg["ms_per_layer_1m"] = ms1
+        cfg["tflops_per_schedule_1m"] = {k_: f1 / (v_ * 1e-3) / 1e12 for k_, v_ in ms1.items()}
+        cfg["steps_1m"] = steps1
+        del outs1, wss1, q1, k1, v1
+        torch.cuda.empty_cache()
+        outs, wss = make_buffers(B, w, q, k)
+
+    # ---- end to end through the host-buffer entry point
+    e2e = None
+    if not args.skip_e2e:
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        oh = torch.empty_like(qh).pin_memory()
+        lh = torch.empty((w.batch, w.hq, w.sq), dtype=torch.float32).pin_memory()
+        need = max(B.host_scratch_size(qh, kh, w.n_chunks, m, w.q_base, w.causal)
+                   for m in (B.PASS_KV, B.PASS_Q))
+        del outs, wss
+        torch.cuda.empty_cache()
+        scratch = torch.empty(need, dtype=torch.uint8, device="cuda")
+
+        def host_step():
+            for m in (B.PASS_KV, B.PASS_Q):
+                B.prefill_host(qh, kh, vh, w.n_chunks, m, oh, lh, scratch, q_base=w.q_base,
+                               causal=w.causal)
+
+        for _ in range(args.warmup):
+            host_step()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            host_step()
+        t_e2e = max_over_ranks(time.perf_counter() - t0, world)
+        in_bytes = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+        out_bytes = oh.numel() * oh.element_size() + lh.numel() * 4
+        e2e = {"value": world * flops_step * args.steps / t_e2e / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 2 * in_bytes, "d2h_bytes_per_step": 2 * out_bytes,
+               "ms_per_step": 1e3 * t_e2e / args.steps,
+               "path": "cpattn_prefill_host (pinned host buffers; copies inside the timed region)"}
+        del scratch
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0 only)
+    cpu_baseline = None
+    if rank == 0:
+        f, dt, threads, rows = oracle_sample(w, args.cpu_rows)
+        cpu_baseline = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                        "sample": f"{args.cpu_rows} seeded query rows x {w.hq} heads of the {w.name} "
+                                  f"workload (full causal key range each), fp64, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded i.i.d. N(0,1) Q/K/V, bf16)", "config": cfg,
+                "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
+                "gpu_launches": len(recs), "clocks": clk}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

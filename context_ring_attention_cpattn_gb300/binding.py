@@ -1,0 +1,231 @@
+"""Thin Python binding of libcpattn.so (argument marshalling only).
+
+Every function here converts torch tensors into ``cpattn_tensor`` views and
+calls the C ABI declared in ``include/cpattn.h``; all arithmetic runs in the
+library's CUDA kernels.  If the library has not been built the first call
+raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+PASS_KV = 1
+PASS_Q = 2
+BF16, FP32 = 0, 1
+ROLE_NAMES = {0: "store", 1: "acc_init", 2: "acc_merge", 3: "acc_final", 4: "partial"}
+KERNEL_NAMES = {1: "attn_tc", 2: "attn_simt", 3: "merge2", 4: "mergeN"}
+
+
+class CpattnTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("b", ctypes.c_int64), ("s", ctypes.c_int64), ("h", ctypes.c_int64),
+                ("d", ctypes.c_int64), ("stride_b", ctypes.c_int64), ("stride_s", ctypes.c_int64),
+                ("stride_h", ctypes.c_int64)]
+
+
+class PlanEntry(ctypes.Structure):
+    _fields_ = [("step", ctypes.c_int32), ("q_chunk", ctypes.c_int32),
+                ("kv_chunk", ctypes.c_int32), ("role", ctypes.c_int32), ("slot", ctypes.c_int32)]
+
+
+class ProfileRecord(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("ms", ctypes.c_float), ("work", ctypes.c_double)]
+
+
+EXPORTED = ["cpattn_partial", "cpattn_merge", "cpattn_prefill_workspace_size", "cpattn_prefill",
+            "cpattn_prefill_plan", "cpattn_prefill_host_scratch_size", "cpattn_prefill_host",
+            "cpattn_status_string", "cpattn_device_status", "cpattn_profile_begin",
+            "cpattn_profile_end"]
+
+_lib = None
+
+
+class CpattnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = lib().cpattn_status_string(status).decode()
+        super().__init__(f"{where}: {msg}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libcpattn.so (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libcpattn.so is not built ({path}); run __graft_entry__.build()")
+    L = ctypes.CDLL(path)
+    T = ctypes.POINTER(CpattnTensor)
+    vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    sz = ctypes.POINTER(ctypes.c_size_t)
+    L.cpattn_partial.argtypes = [T, T, T, i64, i64, i32, f32, T, vp, vp]
+    L.cpattn_merge.argtypes = [T, vp, T, vp, vp]
+    L.cpattn_prefill_workspace_size.argtypes = [T, T, i64, i32, i32, i32, sz]
+    L.cpattn_prefill.argtypes = [T, T, T, i64, i32, i32, i32, f32, T, vp, vp, ctypes.c_size_t, vp]
+    L.cpattn_prefill_plan.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(PlanEntry), i32,
+                                      ctypes.POINTER(ctypes.c_int)]
+    L.cpattn_prefill_host_scratch_size.argtypes = [T, T, i64, i32, i32, i32, i32, sz]
+    L.cpattn_prefill_host.argtypes = [T, T, T, i64, i32, i32, i32, f32, T, vp, vp, ctypes.c_size_t,
+                                      vp]
+    L.cpattn_status_string.argtypes = [i32]
+    L.cpattn_status_string.restype = ctypes.c_char_p
+    L.cpattn_device_status.argtypes = [i32]
+    L.cpattn_profile_begin.argtypes = [i32]
+    L.cpattn_profile_end.argtypes = [ctypes.POINTER(ProfileRecord), i32, ctypes.POINTER(ctypes.c_int)]
+    for name in EXPORTED:
+        if name != "cpattn_status_string":
+            getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise CpattnError(status, where)
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def view(t) -> CpattnTensor:
+    """cpattn_tensor view of a 4-D [b, s, h, d] torch tensor (last dim contiguous)."""
+    if t.dim() != 4:
+        raise ValueError("expected a [b, s, h, d] tensor")
+    if t.shape[3] > 1 and t.stride(3) != 1:
+        raise ValueError("the d dimension must be contiguous")
+    b, s, h, d = t.shape
+    sb, ss, sh, _ = t.stride()
+    return CpattnTensor(t.data_ptr(), _dtype_code(t), 0, b, s, h, d, sb, ss, sh)
+
+
+def _stream(stream=None) -> int:
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def partial(q, k, v, q_off: int = 0, kv_off: int = 0, causal: bool = True, scale=None,
+            out_dtype=None, out=None, lse=None, stream=None):
+    """(O, LSE) of one (Q-chunk, KV-chunk) pair; see cpattn_partial."""
+    import torch
+
+    B, S, H, D = q.shape
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=out_dtype or q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    qv, kv_, vv, ov = view(q), view(k), view(v), view(out)
+    _check(lib().cpattn_partial(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv), int(q_off),
+                                int(kv_off), int(bool(causal)), float(scale or 0.0),
+                                ctypes.byref(ov), lse.data_ptr(), _stream(stream)), "cpattn_partial")
+    return out, lse
+
+
+def merge_(o_a, lse_a, o_b, lse_b, stream=None):
+    """In place: (o_a, lse_a) <- LSE-merge of (o_a, lse_a) and (o_b, lse_b)."""
+    av, bv = view(o_a), view(o_b)
+    _check(lib().cpattn_merge(ctypes.byref(av), lse_a.data_ptr(), ctypes.byref(bv),
+                              lse_b.data_ptr(), _stream(stream)), "cpattn_merge")
+    return o_a, lse_a
+
+
+def workspace_size(q, k, n_chunks: int, mode: int, q_base: int = 0, causal: bool = True) -> int:
+    n = ctypes.c_size_t(0)
+    qv, kv_ = view(q), view(k)
+    _check(lib().cpattn_prefill_workspace_size(ctypes.byref(qv), ctypes.byref(kv_), int(q_base),
+                                               int(n_chunks), int(mode), int(bool(causal)),
+                                               ctypes.byref(n)), "cpattn_prefill_workspace_size")
+    return n.value
+
+
+def prefill(q, k, v, n_chunks: int, mode: int, q_base: int = 0, causal: bool = True, scale=None,
+            out=None, lse=None, workspace=None, out_dtype=None, stream=None):
+    """CP prefill of one attention layer on one GPU; see cpattn_prefill."""
+    import torch
+
+    B, S, H, D = q.shape
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=out_dtype or q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    need = workspace_size(q, k, n_chunks, mode, q_base, causal)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    qv, kv_, vv, ov = view(q), view(k), view(v), view(out)
+    _check(lib().cpattn_prefill(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
+                                int(q_base), int(n_chunks), int(mode), int(bool(causal)),
+                                float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(), ws_ptr,
+                                ws_len, _stream(stream)), "cpattn_prefill")
+    return out, lse
+
+
+def host_scratch_size(q, k, n_chunks, mode, q_base=0, causal=True, out_dtype=None) -> int:
+    n = ctypes.c_size_t(0)
+    qv, kv_ = view(q), view(k)
+    code = _dtype_code(q) if out_dtype is None else (BF16 if str(out_dtype).endswith("bfloat16") else FP32)
+    _check(lib().cpattn_prefill_host_scratch_size(ctypes.byref(qv), ctypes.byref(kv_), int(q_base),
+                                                  int(n_chunks), int(mode), int(bool(causal)),
+                                                  code, ctypes.byref(n)),
+           "cpattn_prefill_host_scratch_size")
+    return n.value
+
+
+def prefill_host(q, k, v, n_chunks, mode, out, lse, dev_scratch, q_base=0, causal=True,
+                 scale=None, stream=None):
+    """End to end from host tensors: H2D copies, prefill, D2H copies, sync."""
+    qv, kv_, vv, ov = view(q), view(k), view(v), view(out)
+    _check(lib().cpattn_prefill_host(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
+                                     int(q_base), int(n_chunks), int(mode), int(bool(causal)),
+                                     float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(),
+                                     dev_scratch.data_ptr(),
+                                     dev_scratch.numel() * dev_scratch.element_size(),
+                                     _stream(stream)), "cpattn_prefill_host")
+    return out, lse
+
+
+def prefill_plan(sq: int, skv: int, n_chunks: int, mode: int, q_base: int = 0,
+                 causal: bool = True):
+    """Launch-order list of (step, q_chunk, kv_chunk, role, slot) (host only)."""
+    n = ctypes.c_int(0)
+    _check(lib().cpattn_prefill_plan(int(sq), int(skv), int(q_base), int(n_chunks), int(mode),
+                                     int(bool(causal)), None, 0, ctypes.byref(n)),
+           "cpattn_prefill_plan")
+    arr = (PlanEntry * max(1, n.value))()
+    _check(lib().cpattn_prefill_plan(int(sq), int(skv), int(q_base), int(n_chunks), int(mode),
+                                     int(bool(causal)), arr, n.value, ctypes.byref(n)),
+           "cpattn_prefill_plan")
+    return [(e.step, e.q_chunk, e.kv_chunk, e.role, e.slot) for e in arr[:n.value]]
+
+
+def device_status(clear: bool = True) -> int:
+    return lib().cpattn_device_status(int(bool(clear)))
+
+
+def profile_begin(capacity: int):
+    _check(lib().cpattn_profile_begin(int(capacity)), "cpattn_profile_begin")
+
+
+def profile_end(capacity: int):
+    recs = (ProfileRecord * capacity)()
+    n = ctypes.c_int(0)
+    _check(lib().cpattn_profile_end(recs, capacity, ctypes.byref(n)), "cpattn_profile_end")
+    return [(KERNEL_NAMES.get(r.kind, str(r.kind)), r.ms, r.work) for r in recs[:min(n.value, capacity)]]

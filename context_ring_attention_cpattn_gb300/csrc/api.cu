@@ -1,0 +1,619 @@
+// C ABI of libcpattn.so: argument checks, the CP ring plan, workspace layout
+// and the step-by-step launch sequence (see include/cpattn.h).
+//
+// The ring emulation follows "Scaling LLM Inference ..." (techreport rewrite,
+// section "Context Parallelism for Million-Token Contexts"): the sequence is
+// split into N chunks, one per CP rank.  Pass-KV keeps Q chunk r on rank r
+// and moves K/V chunks around the ring: at step t rank r holds K/V chunk
+// (r - t) mod N and folds its pair into a running (O, LSE) accumulator.
+// Pass-Q keeps K/V chunk r on rank r and moves the Q chunks: at step t rank r
+// sees Q chunk (r - t) mod N and stores that pair's partial; after the ring
+// every Q chunk's partials are merged by LSE.  On one GPU a "rank" is a pair
+// in a launch, a "send" is a different row offset into the resident tensors,
+// and the N ring steps are N launches back to back on one stream.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+#include <vector>
+
+#include "cpattn_internal.h"
+
+using namespace cpattn;
+
+namespace {
+
+// ----------------------------------------------------------------- checks
+int elem_bytes(int32_t dtype) {
+  return dtype == CPATTN_BF16 ? 2 : (dtype == CPATTN_FP32 ? 4 : 0);
+}
+
+constexpr int64_t kMaxRows = (int64_t)1 << 30;
+
+// Shape, dtype, pointer and stride checks shared by every tensor argument.
+cpattn_status check_view(const cpattn_tensor *t) {
+  if (t == nullptr) return CPATTN_ERR_INVALID_ARG;
+  const int es = elem_bytes(t->dtype);
+  if (es == 0) return CPATTN_ERR_INVALID_ARG;
+  if (t->b < 1 || t->s < 0 || t->h < 1 || t->d < 1) return CPATTN_ERR_INVALID_ARG;
+  if (t->s > kMaxRows || t->b > 65535 || t->h > 65535) return CPATTN_ERR_UNSUPPORTED;
+  if (t->s > 0 && t->data == nullptr) return CPATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(t->data) % 16 != 0) return CPATTN_ERR_INVALID_ARG;
+  if (t->stride_h < 0 || t->stride_s < 0 || t->stride_b < 0) return CPATTN_ERR_INVALID_ARG;
+  if ((t->stride_h * es) % 16 != 0 || (t->stride_s * es) % 16 != 0) return CPATTN_ERR_INVALID_ARG;
+  if (t->b > 1 && (t->stride_b * es) % 16 != 0) return CPATTN_ERR_INVALID_ARG;
+  if (t->h > 1 && t->stride_h < t->d) return CPATTN_ERR_INVALID_ARG;
+  return CPATTN_OK;
+}
+
+// q, k, v consistency.
+cpattn_status check_qkv(const cpattn_tensor *q, const cpattn_tensor *k, const cpattn_tensor *v) {
+  cpattn_status s;
+  if ((s = check_view(q)) != CPATTN_OK) return s;
+  if ((s = check_view(k)) != CPATTN_OK) return s;
+  if ((s = check_view(v)) != CPATTN_OK) return s;
+  if (k->dtype != q->dtype || v->dtype != q->dtype) return CPATTN_ERR_INVALID_ARG;
+  if (k->b != q->b || v->b != q->b) return CPATTN_ERR_INVALID_ARG;
+  if (v->s != k->s || v->h != k->h) return CPATTN_ERR_INVALID_ARG;
+  if (k->d != q->d || v->d != q->d) return CPATTN_ERR_INVALID_ARG;
+  if (q->h % k->h != 0) return CPATTN_ERR_INVALID_ARG;
+  if (q->d != 64 && q->d != 128) return CPATTN_ERR_UNSUPPORTED;
+  return CPATTN_OK;
+}
+
+cpattn_status check_out(const cpattn_tensor *o, const float *lse, const cpattn_tensor *q) {
+  cpattn_status s = check_view(o);
+  if (s != CPATTN_OK) return s;
+  if (o->b != q->b || o->s != q->s || o->h != q->h || o->d != q->d) return CPATTN_ERR_INVALID_ARG;
+  if (q->s > 0 && lse == nullptr) return CPATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(lse) % 4 != 0) return CPATTN_ERR_INVALID_ARG;
+  return CPATTN_OK;
+}
+
+float resolve_scale(float scale, int64_t d) {
+  return scale > 0.f ? scale : (float)(1.0 / sqrt((double)d));
+}
+
+OutView out_view(const cpattn_tensor *o, float *lse) {
+  OutView w;
+  memset(&w, 0, sizeof(w));
+  w.o = o->data;
+  w.lse = lse;
+  w.sb = o->stride_b;
+  w.ss = o->stride_s;
+  w.sh = o->stride_h;
+  w.lb = o->h * o->s;
+  w.lh = o->s;
+  w.f32 = o->dtype == CPATTN_FP32;
+  return w;
+}
+
+void fill_inputs(AttnParams &p, const cpattn_tensor *q, const cpattn_tensor *k,
+                 const cpattn_tensor *v, int causal, float scale) {
+  memset(&p, 0, sizeof(p));
+  p.B = (int32_t)q->b;
+  p.Hq = (int32_t)q->h;
+  p.Hkv = (int32_t)k->h;
+  p.D = (int32_t)q->d;
+  p.causal = causal ? 1 : 0;
+  p.scale = resolve_scale(scale, q->d);
+  p.scale_log2 = (float)((double)p.scale * 1.4426950408889634);
+  p.q = q->data;
+  p.k = k->data;
+  p.v = v->data;
+  p.q_sb = q->stride_b; p.q_ss = q->stride_s; p.q_sh = q->stride_h;
+  p.k_sb = k->stride_b; p.k_ss = k->stride_s; p.k_sh = k->stride_h;
+  p.v_sb = v->stride_b; p.v_ss = v->stride_s; p.v_sh = v->stride_h;
+  p.q_rows_total = q->s;
+  p.kv_rows_total = k->s;
+  p.in_f32 = q->dtype == CPATTN_FP32;
+}
+
+// Number of (query, key) pairs the mask keeps for query rows at positions
+// q0 .. q0+nq-1 against keys at k0 .. k0+nk-1.
+double visible_pairs(int64_t q0, int64_t nq, int64_t k0, int64_t nk, bool causal) {
+  if (nq <= 0 || nk <= 0) return 0.0;
+  if (!causal) return (double)nq * (double)nk;
+  const int64_t a = q0 - k0 + 1;  // keys visible to row i: clamp(a + i, 0, nk)
+  const int64_t lo = std::min<int64_t>(std::max<int64_t>(1 - a, 0), nq);
+  const int64_t hi = std::min<int64_t>(std::max<int64_t>(nk - a, lo), nq);
+  const double ramp = (double)(hi - lo) * (double)a + (double)(lo + hi - 1) * (double)(hi - lo) / 2.0;
+  return ramp + (double)(nq - hi) * (double)nk;
+}
+
+// ----------------------------------------------------------------- profiling
+struct Profiler {
+  bool armed = false;
+  int capacity = 0;
+  int n = 0;
+  std::vector<cudaEvent_t> events;
+  std::vector<int32_t> kinds;
+  std::vector<double> work;
+};
+Profiler g_prof;
+
+void prof_before(cudaStream_t st) {
+  if (g_prof.armed && g_prof.n < g_prof.capacity) cudaEventRecord(g_prof.events[2 * g_prof.n], st);
+}
+void prof_after(cudaStream_t st, int kind, double work) {
+  if (g_prof.armed && g_prof.n < g_prof.capacity) {
+    cudaEventRecord(g_prof.events[2 * g_prof.n + 1], st);
+    g_prof.kinds[g_prof.n] = kind;
+    g_prof.work[g_prof.n] = work;
+    ++g_prof.n;
+  }
+}
+
+// ----------------------------------------------------------------- the plan
+struct Plan {
+  int N = 0;
+  int mode = 0;
+  int64_t Cq = 0, C = 0;
+  std::vector<cpattn_plan_entry> entries;  // launch order
+  std::vector<int> count;                  // non-empty pairs per Q chunk
+  std::vector<int> slot0;                  // Pass-Q: first slot of the chunk (-1: none)
+  int n_slots = 0;
+  bool need_acc = false;                   // Pass-KV needs the accumulator
+};
+
+bool pair_visible(const Plan &pl, int64_t q_base, bool causal, int i, int j) {
+  if (pl.Cq <= 0 || pl.C <= 0) return false;
+  if (!causal) return true;
+  return (int64_t)j * pl.C <= q_base + (int64_t)i * pl.Cq + pl.Cq - 1;
+}
+
+cpattn_status build_plan(int64_t sq, int64_t skv, int64_t q_base, int n_chunks, int mode,
+                         int causal, Plan &pl) {
+  if (n_chunks < 1 || n_chunks > kMaxPairs) return CPATTN_ERR_INVALID_ARG;
+  if (mode != CPATTN_PASS_KV && mode != CPATTN_PASS_Q) return CPATTN_ERR_INVALID_ARG;
+  if (sq < 0 || skv < 0 || sq % n_chunks != 0 || skv % n_chunks != 0) return CPATTN_ERR_INVALID_ARG;
+  if (sq > kMaxRows || skv > kMaxRows || q_base < -kMaxRows * 4 || q_base > kMaxRows * 4)
+    return CPATTN_ERR_UNSUPPORTED;
+  const int N = n_chunks;
+  pl.N = N;
+  pl.mode = mode;
+  pl.Cq = sq / N;
+  pl.C = skv / N;
+  pl.count.assign(N, 0);
+  pl.slot0.assign(N, -1);
+  pl.entries.clear();
+  for (int i = 0; i < N; ++i)
+    for (int j = 0; j < N; ++j) pl.count[i] += pair_visible(pl, q_base, causal, i, j) ? 1 : 0;
+  pl.n_slots = 0;
+  if (mode == CPATTN_PASS_Q) {
+    for (int i = 0; i < N; ++i)
+      if (pl.count[i] >= 2) {
+        pl.slot0[i] = pl.n_slots;
+        pl.n_slots += pl.count[i];
+      }
+  }
+  std::vector<int> seen(N, 0);
+  for (int t = 0; t < N; ++t) {
+    for (int r = 0; r < N; ++r) {
+      const int i = mode == CPATTN_PASS_KV ? r : ((r - t) % N + N) % N;
+      const int j = mode == CPATTN_PASS_KV ? ((r - t) % N + N) % N : r;
+      if (!pair_visible(pl, q_base, causal, i, j)) continue;
+      cpattn_plan_entry e;
+      e.step = t;
+      e.q_chunk = i;
+      e.kv_chunk = j;
+      e.slot = -1;
+      if (pl.count[i] == 1) {
+        e.role = CPATTN_ROLE_STORE;
+      } else if (mode == CPATTN_PASS_KV) {
+        const int k = seen[i]++;
+        e.role = k == 0 ? CPATTN_ROLE_ACC_INIT
+                        : (k == pl.count[i] - 1 ? CPATTN_ROLE_ACC_FINAL : CPATTN_ROLE_ACC_MERGE);
+        pl.need_acc = true;
+      } else {
+        // Rank of j among chunk i's visible KV chunks, ascending.
+        int rank = 0;
+        for (int jj = 0; jj < j; ++jj) rank += pair_visible(pl, q_base, causal, i, jj) ? 1 : 0;
+        e.role = CPATTN_ROLE_PARTIAL;
+        e.slot = pl.slot0[i] + rank;
+      }
+      pl.entries.push_back(e);
+    }
+  }
+  return CPATTN_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t acc_o = 0, acc_lse = 0;      // Pass-KV
+  size_t part_o = 0, part_lse = 0;    // Pass-Q
+  int64_t slot_o_elems = 0, slot_lse_elems = 0;
+  size_t total = 0;
+};
+
+WsLayout ws_layout(const Plan &pl, int64_t B, int64_t sq, int64_t hq, int64_t d) {
+  WsLayout w;
+  size_t off = 0;
+  if (pl.mode == CPATTN_PASS_KV && pl.need_acc) {
+    w.acc_o = off;
+    off = align256(off + (size_t)B * sq * hq * d * 4);
+    w.acc_lse = off;
+    off = align256(off + (size_t)B * hq * sq * 4);
+  }
+  if (pl.mode == CPATTN_PASS_Q && pl.n_slots > 0) {
+    w.slot_o_elems = B * pl.Cq * hq * d;
+    w.slot_lse_elems = B * hq * pl.Cq;
+    w.part_o = off;
+    off = align256(off + (size_t)pl.n_slots * w.slot_o_elems * 4);
+    w.part_lse = off;
+    off = align256(off + (size_t)pl.n_slots * w.slot_lse_elems * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+cudaError_t launch_attn(AttnParams &p, cudaStream_t st, const cpattn_tensor *q) {
+  double vis = 0.0;
+  for (int x = 0; x < p.n_pairs; ++x) {
+    const PairDesc &pd = p.pairs[x];
+    vis += visible_pairs(pd.delta, pd.q_len, 0, pd.kv_len, p.causal != 0);
+  }
+  const double flops = 4.0 * (double)q->d * (double)q->h * (double)q->b * vis;
+  const bool tc = attn_tc_supported(p);
+  prof_before(st);
+  cudaError_t e = tc ? launch_attn_tc(p, st) : launch_attn_simt(p, st);
+  prof_after(st, tc ? CPATTN_KERNEL_ATTN_TC : CPATTN_KERNEL_ATTN_SIMT, flops);
+  return e;
+}
+
+cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const cpattn_tensor *v,
+                           int64_t q_base, int n_chunks, int mode, int causal, float scale,
+                           cpattn_tensor *o, float *lse, void *workspace, size_t ws_bytes,
+                           cudaStream_t st) {
+  cpattn_status s = check_qkv(q, k, v);
+  if (s != CPATTN_OK) return s;
+  if ((s = check_out(o, lse, q)) != CPATTN_OK) return s;
+  Plan pl;
+  if ((s = build_plan(q->s, k->s, q_base, n_chunks, mode, causal, pl)) != CPATTN_OK) return s;
+  const WsLayout wl = ws_layout(pl, q->b, q->s, q->h, q->d);
+  if (wl.total > 0) {
+    if (workspace == nullptr || ws_bytes < wl.total) return CPATTN_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return CPATTN_ERR_WORKSPACE;
+  }
+  if (q->s == 0) return CPATTN_OK;
+  uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+
+  AttnParams p;
+  fill_inputs(p, q, k, v, causal, scale);
+  p.out = out_view(o, lse);
+  if (wl.acc_lse > 0 || (pl.mode == CPATTN_PASS_KV && pl.need_acc)) {
+    p.acc.o = ws + wl.acc_o;
+    p.acc.lse = reinterpret_cast<float *>(ws + wl.acc_lse);
+    p.acc.sh = q->d;
+    p.acc.ss = q->h * q->d;
+    p.acc.sb = q->s * q->h * q->d;
+    p.acc.lh = q->s;
+    p.acc.lb = q->h * q->s;
+    p.acc.f32 = 1;
+  }
+  if (pl.n_slots > 0) {
+    p.part.o = ws + wl.part_o;
+    p.part.lse = reinterpret_cast<float *>(ws + wl.part_lse);
+    p.part.sh = q->d;
+    p.part.ss = q->h * q->d;
+    p.part.sb = pl.Cq * q->h * q->d;
+    p.part.lh = pl.Cq;
+    p.part.lb = q->h * pl.Cq;
+    p.part.f32 = 1;
+    p.part_o_stride = wl.slot_o_elems;
+    p.part_lse_stride = wl.slot_lse_elems;
+  }
+
+  // One launch per ring step; pairs ordered by work, largest first.
+  size_t e0 = 0;
+  for (int t = 0; t < pl.N; ++t) {
+    size_t e1 = e0;
+    while (e1 < pl.entries.size() && pl.entries[e1].step == t) ++e1;
+    if (e1 == e0) continue;
+    struct Item { PairDesc pd; double work; };
+    std::vector<Item> items;
+    for (size_t x = e0; x < e1; ++x) {
+      const cpattn_plan_entry &e = pl.entries[x];
+      Item it;
+      memset(&it.pd, 0, sizeof(it.pd));
+      it.pd.q_row0 = (int32_t)(e.q_chunk * pl.Cq);
+      it.pd.q_len = (int32_t)pl.Cq;
+      it.pd.kv_row0 = (int32_t)(e.kv_chunk * pl.C);
+      it.pd.kv_len = (int32_t)pl.C;
+      it.pd.delta = q_base + (int64_t)e.q_chunk * pl.Cq - (int64_t)e.kv_chunk * pl.C;
+      it.pd.mode = e.role;
+      it.pd.slot = e.slot;
+      it.work = visible_pairs(it.pd.delta, pl.Cq, 0, pl.C, causal != 0);
+      items.push_back(it);
+    }
+    std::stable_sort(items.begin(), items.end(),
+                     [](const Item &a, const Item &b) { return a.work > b.work; });
+    p.n_pairs = (int32_t)items.size();
+    for (size_t x = 0; x < items.size(); ++x) p.pairs[x] = items[x].pd;
+    if (launch_attn(p, st, q) != cudaSuccess) return CPATTN_ERR_CUDA;
+    e0 = e1;
+  }
+
+  // Pass-Q merge of partials, and empty rows of chunks no key reaches.
+  MergeNParams mp;
+  memset(&mp, 0, sizeof(mp));
+  mp.B = (int32_t)q->b;
+  mp.H = (int32_t)q->h;
+  mp.D = (int32_t)q->d;
+  mp.chunk_rows = (int32_t)pl.Cq;
+  mp.out = p.out;
+  mp.part = p.part;
+  mp.part_o_stride = p.part_o_stride;
+  mp.part_lse_stride = p.part_lse_stride;
+  double bytes = 0.0;
+  const double row_bytes = (double)q->b * pl.Cq * q->h * (q->d * 4.0 + 4.0);
+  const double out_bytes = (double)q->b * pl.Cq * q->h * (q->d * elem_bytes(o->dtype) + 4.0);
+  for (int i = 0; i < pl.N; ++i) {
+    const bool merge = pl.mode == CPATTN_PASS_Q && pl.count[i] >= 2;
+    if (!merge && pl.count[i] != 0) continue;
+    mp.item_row0[mp.n_items] = (int32_t)(i * pl.Cq);
+    mp.item_slot0[mp.n_items] = merge ? pl.slot0[i] : 0;
+    mp.item_count[mp.n_items] = merge ? pl.count[i] : 0;
+    bytes += (merge ? pl.count[i] * row_bytes : 0.0) + out_bytes;
+    ++mp.n_items;
+  }
+  if (mp.n_items > 0) {
+    prof_before(st);
+    cudaError_t e = launch_merge_n(mp, st);
+    prof_after(st, CPATTN_KERNEL_MERGEN, bytes);
+    if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  }
+  return CPATTN_OK;
+}
+
+size_t tensor_bytes(const cpattn_tensor *t) {
+  return (size_t)t->b * t->s * t->h * t->d * elem_bytes(t->dtype);
+}
+
+bool is_contiguous(const cpattn_tensor *t) {
+  return t->stride_h == t->d && t->stride_s == t->h * t->d &&
+         (t->b == 1 || t->stride_b == t->s * t->h * t->d);
+}
+
+cpattn_tensor dense_like(const cpattn_tensor *t, void *data, int32_t dtype) {
+  cpattn_tensor r = *t;
+  r.data = data;
+  r.dtype = dtype;
+  r.stride_h = t->d;
+  r.stride_s = t->h * t->d;
+  r.stride_b = t->s * t->h * t->d;
+  return r;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *cpattn_status_string(cpattn_status s) {
+  switch (s) {
+    case CPATTN_OK: return "CPATTN_OK";
+    case CPATTN_ERR_INVALID_ARG: return "CPATTN_ERR_INVALID_ARG: bad argument";
+    case CPATTN_ERR_UNSUPPORTED: return "CPATTN_ERR_UNSUPPORTED: shape or dtype not supported";
+    case CPATTN_ERR_WORKSPACE: return "CPATTN_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case CPATTN_ERR_CUDA: return "CPATTN_ERR_CUDA: a CUDA call or launch failed";
+    case CPATTN_ERR_TIMEOUT: return "CPATTN_ERR_TIMEOUT: a kernel-side wait gave up";
+  }
+  return "CPATTN: unknown status";
+}
+
+cpattn_status cpattn_partial(const cpattn_tensor *q, const cpattn_tensor *k,
+                             const cpattn_tensor *v, int64_t q_off, int64_t kv_off, int causal,
+                             float scale, cpattn_tensor *o, float *lse, void *stream) {
+  try {
+    cpattn_status s = check_qkv(q, k, v);
+    if (s != CPATTN_OK) return s;
+    if ((s = check_out(o, lse, q)) != CPATTN_OK) return s;
+    if (q_off < -kMaxRows * 4 || q_off > kMaxRows * 4 || kv_off < -kMaxRows * 4 ||
+        kv_off > kMaxRows * 4)
+      return CPATTN_ERR_UNSUPPORTED;
+    if (q->s == 0) return CPATTN_OK;
+    AttnParams p;
+    fill_inputs(p, q, k, v, causal, scale);
+    p.out = out_view(o, lse);
+    p.n_pairs = 1;
+    p.pairs[0].q_row0 = 0;
+    p.pairs[0].q_len = (int32_t)q->s;
+    p.pairs[0].kv_row0 = 0;
+    p.pairs[0].kv_len = (int32_t)k->s;
+    p.pairs[0].delta = q_off - kv_off;
+    p.pairs[0].mode = kStore;
+    p.pairs[0].slot = -1;
+    return launch_attn(p, reinterpret_cast<cudaStream_t>(stream), q) == cudaSuccess
+               ? CPATTN_OK
+               : CPATTN_ERR_CUDA;
+  } catch (...) {
+    return CPATTN_ERR_INVALID_ARG;
+  }
+}
+
+cpattn_status cpattn_merge(cpattn_tensor *o_a, float *lse_a, const cpattn_tensor *o_b,
+                           const float *lse_b, void *stream) {
+  cpattn_status s = check_view(o_a);
+  if (s != CPATTN_OK) return s;
+  if ((s = check_view(o_b)) != CPATTN_OK) return s;
+  if (o_a->dtype != o_b->dtype || o_a->b != o_b->b || o_a->s != o_b->s || o_a->h != o_b->h ||
+      o_a->d != o_b->d)
+    return CPATTN_ERR_INVALID_ARG;
+  if (o_a->d != 64 && o_a->d != 128) return CPATTN_ERR_UNSUPPORTED;
+  if (o_a->s > 0 && (lse_a == nullptr || lse_b == nullptr)) return CPATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(lse_a) % 4 || reinterpret_cast<uintptr_t>(lse_b) % 4)
+    return CPATTN_ERR_INVALID_ARG;
+  if (o_a->s == 0) return CPATTN_OK;
+  Merge2Params p;
+  memset(&p, 0, sizeof(p));
+  p.B = (int32_t)o_a->b;
+  p.S = (int32_t)o_a->s;
+  p.H = (int32_t)o_a->h;
+  p.D = (int32_t)o_a->d;
+  p.a = out_view(o_a, lse_a);
+  p.b = out_view(o_b, const_cast<float *>(lse_b));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const double bytes = 3.0 * (double)o_a->b * o_a->s * o_a->h * (o_a->d * elem_bytes(o_a->dtype) + 4.0);
+  prof_before(st);
+  cudaError_t e = launch_merge_2(p, st);
+  prof_after(st, CPATTN_KERNEL_MERGE2, bytes);
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+cpattn_status cpattn_prefill_workspace_size(const cpattn_tensor *q, const cpattn_tensor *k,
+                                            int64_t q_base, int n_chunks, int mode, int causal,
+                                            size_t *bytes) {
+  try {
+    if (bytes == nullptr) return CPATTN_ERR_INVALID_ARG;
+    cpattn_status s = check_view(q);
+    if (s != CPATTN_OK) return s;
+    if ((s = check_view(k)) != CPATTN_OK) return s;
+    Plan pl;
+    if ((s = build_plan(q->s, k->s, q_base, n_chunks, mode, causal, pl)) != CPATTN_OK) return s;
+    *bytes = ws_layout(pl, q->b, q->s, q->h, q->d).total;
+    return CPATTN_OK;
+  } catch (...) {
+    return CPATTN_ERR_INVALID_ARG;
+  }
+}
+
+cpattn_status cpattn_prefill(const cpattn_tensor *q, const cpattn_tensor *k,
+                             const cpattn_tensor *v, int64_t q_base, int n_chunks, int mode,
+                             int causal, float scale, cpattn_tensor *o, float *lse,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+  try {
+    return prefill_impl(q, k, v, q_base, n_chunks, mode, causal, scale, o, lse, workspace,
+                        workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+  } catch (...) {
+    return CPATTN_ERR_INVALID_ARG;
+  }
+}
+
+cpattn_status cpattn_prefill_plan(int64_t sq, int64_t skv, int64_t q_base, int n_chunks, int mode,
+                                  int causal, cpattn_plan_entry *entries, int capacity,
+                                  int *n_entries) {
+  try {
+    if (n_entries == nullptr || capacity < 0 || (capacity > 0 && entries == nullptr))
+      return CPATTN_ERR_INVALID_ARG;
+    Plan pl;
+    cpattn_status s = build_plan(sq, skv, q_base, n_chunks, mode, causal, pl);
+    if (s != CPATTN_OK) return s;
+    *n_entries = (int)pl.entries.size();
+    for (int x = 0; x < capacity && x < (int)pl.entries.size(); ++x) entries[x] = pl.entries[x];
+    return CPATTN_OK;
+  } catch (...) {
+    return CPATTN_ERR_INVALID_ARG;
+  }
+}
+
+cpattn_status cpattn_prefill_host_scratch_size(const cpattn_tensor *q, const cpattn_tensor *k,
+                                               int64_t q_base, int n_chunks, int mode, int causal,
+                                               int out_dtype, size_t *bytes) {
+  if (bytes == nullptr || elem_bytes(out_dtype) == 0) return CPATTN_ERR_INVALID_ARG;
+  size_t ws = 0;
+  cpattn_status s = cpattn_prefill_workspace_size(q, k, q_base, n_chunks, mode, causal, &ws);
+  if (s != CPATTN_OK) return s;
+  const size_t o_bytes = (size_t)q->b * q->s * q->h * q->d * elem_bytes(out_dtype);
+  *bytes = align256(tensor_bytes(q)) + 2 * align256(tensor_bytes(k)) + align256(o_bytes) +
+           align256((size_t)q->b * q->h * q->s * 4) + ws;
+  return CPATTN_OK;
+}
+
+cpattn_status cpattn_prefill_host(const cpattn_tensor *q, const cpattn_tensor *k,
+                                  const cpattn_tensor *v, int64_t q_base, int n_chunks, int mode,
+                                  int causal, float scale, cpattn_tensor *o, float *lse,
+                                  void *dev_scratch, size_t scratch_bytes, void *stream) {
+  try {
+    cpattn_status s = check_qkv(q, k, v);
+    if (s != CPATTN_OK) return s;
+    if ((s = check_out(o, lse, q)) != CPATTN_OK) return s;
+    if (!is_contiguous(q) || !is_contiguous(k) || !is_contiguous(v) || !is_contiguous(o))
+      return CPATTN_ERR_INVALID_ARG;
+    size_t need = 0;
+    if ((s = cpattn_prefill_host_scratch_size(q, k, q_base, n_chunks, mode, causal, o->dtype,
+                                              &need)) != CPATTN_OK)
+      return s;
+    if (dev_scratch == nullptr || scratch_bytes < need ||
+        reinterpret_cast<uintptr_t>(dev_scratch) % 256 != 0)
+      return CPATTN_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *base = reinterpret_cast<uint8_t *>(dev_scratch);
+    size_t off = 0;
+    auto take = [&](size_t n) { uint8_t *r = base + off; off += align256(n); return r; };
+    const size_t o_bytes = tensor_bytes(o);
+    const size_t lse_bytes = (size_t)q->b * q->h * q->s * 4;
+    cpattn_tensor dq = dense_like(q, take(tensor_bytes(q)), q->dtype);
+    cpattn_tensor dk = dense_like(k, take(tensor_bytes(k)), k->dtype);
+    cpattn_tensor dv = dense_like(v, take(tensor_bytes(v)), v->dtype);
+    cpattn_tensor dout = dense_like(o, take(o_bytes), o->dtype);
+    float *dlse = reinterpret_cast<float *>(take(lse_bytes));
+    void *ws = base + off;
+    const size_t ws_bytes = scratch_bytes - off;
+    if (cudaMemcpyAsync(dq.data, q->data, tensor_bytes(q), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(dk.data, k->data, tensor_bytes(k), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(dv.data, v->data, tensor_bytes(v), cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return CPATTN_ERR_CUDA;
+    s = prefill_impl(&dq, &dk, &dv, q_base, n_chunks, mode, causal, scale, &dout, dlse, ws,
+                     ws_bytes, st);
+    if (s != CPATTN_OK) return s;
+    if (cudaMemcpyAsync(o->data, dout.data, o_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(lse, dlse, lse_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return CPATTN_ERR_CUDA;
+    return cudaStreamSynchronize(st) == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+  } catch (...) {
+    return CPATTN_ERR_INVALID_ARG;
+  }
+}
+
+cpattn_status cpattn_device_status(int clear) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return CPATTN_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  const unsigned int v = attn_tc_read_status(clear != 0, &e);
+  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  return v ? CPATTN_ERR_TIMEOUT : CPATTN_OK;
+}
+
+cpattn_status cpattn_profile_begin(int capacity) {
+  try {
+    if (capacity < 1 || g_prof.armed) return CPATTN_ERR_INVALID_ARG;
+    g_prof.events.assign(2 * capacity, nullptr);
+    for (auto &ev : g_prof.events)
+      if (cudaEventCreate(&ev) != cudaSuccess) return CPATTN_ERR_CUDA;
+    g_prof.kinds.assign(capacity, 0);
+    g_prof.work.assign(capacity, 0.0);
+    g_prof.capacity = capacity;
+    g_prof.n = 0;
+    g_prof.armed = true;
+    return CPATTN_OK;
+  } catch (...) {
+    return CPATTN_ERR_INVALID_ARG;
+  }
+}
+
+cpattn_status cpattn_profile_end(cpattn_profile_record *records, int capacity, int *n_records) {
+  if (!g_prof.armed) return CPATTN_ERR_INVALID_ARG;
+  cpattn_status s = CPATTN_OK;
+  const int n = g_prof.n;
+  if (n_records) *n_records = n;
+  if (n > 0 && cudaEventSynchronize(g_prof.events[2 * n - 1]) != cudaSuccess) s = CPATTN_ERR_CUDA;
+  for (int x = 0; x < n && x < capacity && records && s == CPATTN_OK; ++x) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_prof.events[2 * x], g_prof.events[2 * x + 1]) != cudaSuccess)
+      s = CPATTN_ERR_CUDA;
+    records[x].kind = g_prof.kinds[x];
+    records[x].ms = ms;
+    records[x].work = g_prof.work[x];
+  }
+  for (auto ev : g_prof.events)
+    if (ev) cudaEventDestroy(ev);
+  g_prof.events.clear();
+  g_prof.armed = false;
+  g_prof.n = 0;
+  return s;
+}
+
+}  // extern "C"

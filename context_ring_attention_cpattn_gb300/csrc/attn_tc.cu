@@ -1,0 +1,611 @@
+// Partial attention of (Q-chunk, KV-chunk) pairs on the 5th-generation tensor
+// cores of sm_103a (tcgen05 + TMEM + TMA), bf16 inputs, head_dim 128.
+//
+// What one pair computes: the per-rank step of context-parallel ring
+// attention ("Scaling LLM Inference ...", techreport rewrite, section
+// "Context Parallelism for Million-Token Contexts", Pass-KV / Pass-Q bullets;
+// the pages name only "a fast attention kernel" and give no design):
+//   s_ij = scale * q_i . k_j  for keys with kv_pos(j) <= q_pos(i) (causal),
+//   LSE_i = log sum_j exp(s_ij),  O_i = sum_j exp(s_ij - LSE_i) v_j,
+// with the result routed by the pair's role (see epilogue.cuh).
+//
+// Design (one CTA = one 128-row query tile of NT heads that share a kv head):
+//   warps 0 .. 4*NT-1  softmax: warpgroup t owns tile t, one thread per row
+//                      (TMEM lane), online softmax in the exp2 domain
+//   warp 4*NT          TMA producer: Q once, then K_j / V_j tiles into a
+//                      2-stage ring (128-byte swizzle, 128 x 64 boxes)
+//   warp 4*NT+1        MMA issuer (one thread): S_t = Q_t K_j^T (SMEM x SMEM),
+//                      O_t += P_t V_j (P from TMEM, V from SMEM), fp32 in TMEM
+// TMEM columns: S_t at 128 t, O_t at 128 (NT + t); P_t (bf16 pairs) overwrites
+// the first 64 columns of S_t.  Before S_t(j+1) is written the issuer waits for
+// O_t += P_t(j) V_j to complete (the two MMAs have different accumulators, so
+// their order is not implied).
+// Causal block skip: a tile loads only keys [0, kv_end) where kv_end is the
+// last valid row's limit; only tiles past the first row's limit are masked.
+// Lazy rescale: the running max moves only when it grows by more than 2^8;
+// normalisation by the row sum at the end makes the result exact either way.
+//
+// Every mbarrier wait is bounded (about 2 s of global time); a wait that gives
+// up records CPATTN_ERR_TIMEOUT in a device status word, the CTA drains its
+// own copies and MMAs, frees its TMEM and returns without writing output.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "cpattn_internal.h"
+#include "epilogue.cuh"
+#include "tmem_ldst.cuh"
+
+namespace cpattn {
+
+__device__ unsigned int g_attn_tc_status;
+
+namespace {
+
+constexpr int kBM = 128;                  // query rows per tile (TMEM lanes)
+constexpr int kBN = 128;                  // keys per tile
+constexpr int kD = 128;                   // head dim
+constexpr int kStages = 2;                // K and V ring depth
+constexpr int kBoxBytes = 128 * 128;      // 128 rows x 64 bf16 (one swizzle span)
+constexpr int kTileBytes = 2 * kBoxBytes; // 128 x 128 bf16
+constexpr float kRescaleLog2 = 8.0f;      // lazy-rescale threshold (log2 units)
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+template <int NT>
+struct Layout {
+  static constexpr int kThreads = (4 * NT + 2) * 32;
+  static constexpr int kTmaWarp = 4 * NT;
+  static constexpr int kMmaWarp = 4 * NT + 1;
+  static constexpr int kTmemCols = NT == 2 ? 512 : 256;
+  static constexpr int q_off = 0;
+  static constexpr int k_off = q_off + NT * kTileBytes;
+  static constexpr int v_off = k_off + kStages * kTileBytes;
+  static constexpr int bar_off = v_off + kStages * kTileBytes;
+  // barrier indices
+  static constexpr int b_qfull = 0;
+  static constexpr int b_kfull = 1;
+  static constexpr int b_kempty = b_kfull + kStages;
+  static constexpr int b_vfull = b_kempty + kStages;
+  static constexpr int b_vempty = b_vfull + kStages;
+  static constexpr int b_sfull = b_vempty + kStages;
+  static constexpr int b_pready = b_sfull + NT;
+  static constexpr int b_pvdone = b_pready + NT;
+  static constexpr int b_drain = b_pvdone + NT;
+  static constexpr int n_bars = b_drain + 1;
+  static constexpr int tmem_slot_off = bar_off + n_bars * 8;
+  static constexpr int abort_off = tmem_slot_off + 4;
+  static constexpr int bytes = abort_off + 4;
+  static constexpr int alloc_bytes = bytes + 1024;  // room to align the base to 1024
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for the phase with the given parity.  Returns false if the
+// CTA's abort flag is raised (when honour_abort) or the time limit passes; a
+// timeout raises the abort flag and records the device status.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         bool honour_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (honour_abort && *abort_flag) return false;
+      if (global_ns() - t0 > kWaitNs) {
+        *abort_flag = 1;
+        atomicOr(&g_attn_tc_status, 1u);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// D(tmem) (+)= A(smem) * B(smem)
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D(tmem) (+)= A(tmem) * B(smem)
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4)                                // D format: f32
+         | (1u << 7)                              // A format: bf16
+         | (1u << 10)                             // B format: bf16
+         | (0u << 15)                             // A K-major
+         | ((b_mn_major ? 1u : 0u) << 16)         // B K-major (0) or MN-major (1)
+         | ((uint32_t)(N >> 3) << 17)             // N / 8
+         | ((uint32_t)(M >> 4) << 24);            // M / 16
+}
+constexpr uint32_t kIdescQK = make_idesc(kBM, kBN, false);
+constexpr uint32_t kIdescPV = make_idesc(kBM, kD, true);
+
+// Shared-memory matrix descriptor, 128-byte swizzle.
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;   // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;   // SWIZZLE_128B
+  return d;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&t);
+}
+
+// ---------------------------------------------------------------- kernel
+template <int NT>
+__global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnParams p) {
+  using L = Layout<NT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int idx) -> uint32_t { return sb + L::bar_off + 8 * idx; };
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::abort_off);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work item: (pair, query tile, head group, batch)
+  int pi = 0;
+  while (pi + 1 < p.n_pairs && (int)blockIdx.x >= p.pairs[pi + 1].cta_begin) ++pi;
+  const PairDesc &pd = p.pairs[pi];
+  int local = (int)blockIdx.x - pd.cta_begin;
+  const int n_hg = p.Hq / NT;
+  const int hg = local % n_hg;
+  local /= n_hg;
+  const int b = local % p.B;
+  const int qt = pd.n_qtiles - 1 - local / p.B;  // longest tiles first
+  const int h0 = hg * NT;
+  const int hk = h0 / (p.Hq / p.Hkv);
+  const int i0 = qt * kBM;
+  const int q_rows = min(kBM, pd.q_len - i0);
+
+  // Keys [0, kv_end) are visible to some row of the tile; keys [0, full_end)
+  // to every row.
+  int64_t kv_end = pd.kv_len, full_end = pd.kv_len;
+  if (p.causal) {
+    const int64_t last_lim = (int64_t)(i0 + q_rows - 1) + pd.delta + 1;
+    const int64_t first_lim = (int64_t)i0 + pd.delta + 1;
+    kv_end = last_lim < kv_end ? last_lim : kv_end;
+    full_end = first_lim < full_end ? first_lim : full_end;
+  }
+  if (kv_end < 0) kv_end = 0;
+  if (full_end < 0) full_end = 0;
+  const int n_kv = (int)((kv_end + kBN - 1) / kBN);
+  const int n_unmasked = (int)(full_end / kBN);
+
+  // ---- setup
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::b_qfull), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(L::b_kfull + s), 1);
+      mbar_init(bar(L::b_kempty + s), 1);
+      mbar_init(bar(L::b_vfull + s), 1);
+      mbar_init(bar(L::b_vempty + s), 1);
+    }
+    for (int t = 0; t < NT; ++t) {
+      mbar_init(bar(L::b_sfull + t), 1);
+      mbar_init(bar(L::b_pready + t), 4);
+      mbar_init(bar(L::b_pvdone + t), 1);
+    }
+    mbar_init(bar(L::b_drain), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == L::kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == L::kMmaWarp) {
+    tmem_alloc(sb + L::tmem_slot_off, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::tmem_slot_off);
+
+  if (warp == L::kTmaWarp) {
+    // ================================================= TMA producer
+    if (lane == 0 && n_kv > 0) {
+      int issued_k[kStages] = {0}, issued_v[kStages] = {0};
+      bool q_issued = false, ok = true;
+      mbar_expect_tx(bar(L::b_qfull), NT * kTileBytes);
+      for (int t = 0; t < NT; ++t)
+        for (int half = 0; half < 2; ++half)
+          tma_load_4d(sb + L::q_off + t * kTileBytes + half * kBoxBytes, &tm_q, bar(L::b_qfull),
+                      half * 64, h0 + t, pd.q_row0 + i0, b);
+      q_issued = true;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int st = j % kStages;
+        const int kv_row = pd.kv_row0 + j * kBN;
+        if (j >= kStages && !wait_bar(bar(L::b_kempty + st), ((j / kStages) - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(bar(L::b_kfull + st), kTileBytes);
+        for (int half = 0; half < 2; ++half)
+          tma_load_4d(sb + L::k_off + st * kTileBytes + half * kBoxBytes, &tm_k,
+                      bar(L::b_kfull + st), half * 64, hk, kv_row, b);
+        ++issued_k[st];
+        if (j >= kStages && !wait_bar(bar(L::b_vempty + st), ((j / kStages) - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(bar(L::b_vfull + st), kTileBytes);
+        for (int half = 0; half < 2; ++half)
+          tma_load_4d(sb + L::v_off + st * kTileBytes + half * kBoxBytes, &tm_v,
+                      bar(L::b_vfull + st), half * 64, hk, kv_row, b);
+        ++issued_v[st];
+      }
+      if (!ok) {
+        // Let the copies already in flight land before the CTA exits.
+        if (q_issued) wait_bar(bar(L::b_qfull), 0, abort_flag, false);
+        for (int s = 0; s < kStages; ++s) {
+          if (issued_k[s] > 0) wait_bar(bar(L::b_kfull + s), (issued_k[s] - 1) & 1, abort_flag, false);
+          if (issued_v[s] > 0) wait_bar(bar(L::b_vfull + s), (issued_v[s] - 1) & 1, abort_flag, false);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == L::kMmaWarp) {
+    // ================================================= MMA issuer
+    if (lane == 0 && n_kv > 0) {
+      bool ok = wait_bar(bar(L::b_qfull), 0, abort_flag);
+      auto issue_qk = [&](int t, int st) {
+        const uint32_t qa = sb + L::q_off + t * kTileBytes;
+        const uint32_t ka = sb + L::k_off + st * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_ss(tmem + t * 128, make_sdesc(qa + off, 16, 1024), make_sdesc(ka + off, 16, 1024),
+                 kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int st, bool accumulate) {
+        const uint32_t va = sb + L::v_off + st * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          mma_ts(tmem + (NT + t) * 128, tmem + t * 128 + kk * 8,
+                 make_sdesc(va + kk * 16 * 128, kBoxBytes, 1024), kIdescPV,
+                 (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+      if (ok) ok = wait_bar(bar(L::b_kfull + 0), 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < NT; ++t) {
+          issue_qk(t, 0);
+          mma_commit(bar(L::b_sfull + t));
+        }
+        mma_commit(bar(L::b_kempty + 0));
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int st = j % kStages;
+        const int st1 = (j + 1) % kStages;
+        const bool more = j + 1 < n_kv;
+        if (!wait_bar(bar(L::b_vfull + st), (j / kStages) & 1, abort_flag)) { ok = false; break; }
+        if (more && !wait_bar(bar(L::b_kfull + st1), ((j + 1) / kStages) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        for (int t = 0; t < NT && ok; ++t) {
+          if (!wait_bar(bar(L::b_pready + t), j & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(t, st, j > 0);
+          mma_commit(bar(L::b_pvdone + t));
+          if (t == NT - 1) mma_commit(bar(L::b_vempty + st));
+          if (more) {
+            // S_t(j+1) overwrites the columns that hold P_t(j).
+            if (!wait_bar(bar(L::b_pvdone + t), j & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            issue_qk(t, st1);
+            mma_commit(bar(L::b_sfull + t));
+            if (t == NT - 1) mma_commit(bar(L::b_kempty + st1));
+          }
+        }
+      }
+      if (!ok) {
+        mma_commit(bar(L::b_drain));
+        wait_bar(bar(L::b_drain), 0, abort_flag, false);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================================================= softmax warpgroups
+    const int t = warp >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // row in the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + t * 128;
+    const uint32_t t_o = tmem + lane_off + (NT + t) * 128;
+    int64_t lim = pd.kv_len;  // this row's visible keys: [0, lim)
+    if (p.causal) {
+      const int64_t c = (int64_t)(i0 + r) + pd.delta + 1;
+      lim = c < lim ? c : lim;
+    }
+    const float sl2 = p.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      // Warp-uniform outcome: the TMEM accesses below are warp-collective.
+      if (!__all_sync(0xffffffffu, wait_bar(bar(L::b_sfull + t), j & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld_x128(t_s, sr);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < kBN; ++c) s[c] = __uint_as_float(sr[c]);
+      if (j >= n_unmasked) {
+        int64_t nv = lim - (int64_t)j * kBN;
+        const int nvis = nv < 0 ? 0 : (nv > kBN ? kBN : (int)nv);
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if (c >= nvis) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+      const float m_new = fmaxf(m_run, mx * sl2);
+      const bool grow = m_new > m_run + kRescaleLog2;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ex2(m_run - m_new);  // 0 when m_run = -inf
+        l_run *= alpha;
+      }
+      const bool rescale_o = grow && (m_run != -INFINITY) && j > 0;
+      if (grow) m_run = m_new;
+      if (__any_sync(0xffffffffu, rescale_o)) {
+        const float a = rescale_o ? alpha : 1.f;
+#pragma unroll
+        for (int cc = 0; cc < kD / 32; ++cc) {
+          uint32_t ov[32];
+          tmem_ld_x32(t_o + cc * 32, ov);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * a);
+          tmem_st_x32(t_o + cc * 32, ov);
+        }
+      }
+      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+      uint32_t pk[64];
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBN; c += 2) {
+        const float p0 = ex2(fmaf(s[c], sl2, neg_m));
+        const float p1 = ex2(fmaf(s[c + 1], sl2, neg_m));
+        lsum += p0 + p1;
+        pk[c >> 1] = pack_bf16(p0, p1);
+      }
+      l_run += lsum;
+      tmem_st_x64(t_s, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::b_pready + t));
+    }
+
+    // ---- epilogue: O_t / l, LSE, routed by the pair's role
+    if (ok && n_kv > 0) {
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::b_pvdone + t), (n_kv - 1) & 1, abort_flag));
+      tc_fence_after();
+    }
+    if (__all_sync(0xffffffffu, ok && !*abort_flag)) {
+      const bool valid = r < q_rows;
+      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      RowSink sink;
+      if (valid) sink.init(p, pd, b, h0 + t, i0 + r, lse, true);
+#pragma unroll 1
+      for (int cc = 0; cc < kD / 32; ++cc) {
+        float ov[32];
+        if (n_kv > 0) {
+          uint32_t raw[32];
+          tmem_ld_x32(t_o + cc * 32, raw);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) ov[x] = __uint_as_float(raw[x]) * inv_l;
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) ov[x] = 0.f;
+        }
+        if (valid) sink.put<32>(cc * 32, ov);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == L::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// [b, s, h, d] bf16 view -> 4-D tensor map (d, h, s, b), box 64 x 1 x 128 x 1.
+bool make_map(CUtensorMap *map, const void *base, int64_t B, int64_t S, int64_t H, int64_t D,
+              int64_t sb, int64_t ss, int64_t sh) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  if (B == 1) sb = S * ss > 0 ? S * ss : 8;  // unused extent: any legal stride
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)sh * 2, (cuuint64_t)ss * 2, (cuuint64_t)sb * 2};
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int NT>
+cudaError_t launch_nt(AttnParams &p, cudaStream_t stream) {
+  using L = Layout<NT>;
+  int total = 0;
+  for (int x = 0; x < p.n_pairs; ++x) {
+    PairDesc &pd = p.pairs[x];
+    pd.n_qtiles = (pd.q_len + kBM - 1) / kBM;
+    pd.cta_begin = total;
+    total += pd.n_qtiles * (p.Hq / NT) * p.B;
+  }
+  p.total_ctas = total;
+  if (total == 0) return cudaSuccess;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, p.q, p.B, p.q_rows_total, p.Hq, kD, p.q_sb, p.q_ss, p.q_sh) ||
+      !make_map(&mk, p.k, p.B, p.kv_rows_total, p.Hkv, kD, p.k_sb, p.k_ss, p.k_sh) ||
+      !make_map(&mv, p.v, p.B, p.kv_rows_total, p.Hkv, kD, p.v_sb, p.v_ss, p.v_sh))
+    return cudaErrorInvalidValue;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::alloc_bytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  attn_tc_kernel<NT><<<total, L::kThreads, L::alloc_bytes, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attn_tc_supported(const AttnParams &p) {
+  return !p.in_f32 && p.D == kD && p.q_rows_total > 0 && p.kv_rows_total > 0;
+}
+
+cudaError_t launch_attn_tc(AttnParams &p, cudaStream_t stream) {
+  const int g = p.Hq / p.Hkv;
+  if (g % 2 == 0) return launch_nt<2>(p, stream);
+  return launch_nt<1>(p, stream);
+}
+
+unsigned int attn_tc_read_status(bool clear, cudaError_t *err) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_attn_tc_status, sizeof(v));
+  if (e == cudaSuccess && clear) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_attn_tc_status, &zero, sizeof(zero));
+  }
+  if (err) *err = e;
+  return v;
+}
+
+}  // namespace cpattn

@@ -1,0 +1,98 @@
+// Internal structures shared by the C ABI layer (api.cu) and the kernels.
+// Nothing here is part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/cpattn.h"
+
+namespace cpattn {
+
+constexpr int kMaxPairs = 64;  // pairs per launch = ranks per ring step (n_chunks <= 64)
+
+// Where a pair's result goes (mirrors cpattn_role).
+enum PairMode : int32_t {
+  kStore = CPATTN_ROLE_STORE,
+  kAccInit = CPATTN_ROLE_ACC_INIT,
+  kAccMerge = CPATTN_ROLE_ACC_MERGE,
+  kAccFinal = CPATTN_ROLE_ACC_FINAL,
+  kPartial = CPATTN_ROLE_PARTIAL,
+};
+
+// A strided [b, s, h, d] output view plus its LSE [b, h, s] view.
+struct OutView {
+  void *o;          // bf16 or fp32
+  float *lse;
+  int64_t sb, ss, sh;  // element strides of o
+  int64_t lb, lh;      // element strides of lse (row stride 1)
+  int32_t f32;         // 1: o is fp32, 0: bf16
+  int32_t pad;
+};
+
+// One (Q-chunk, KV-chunk) pair of a launch.
+struct PairDesc {
+  int32_t q_row0, q_len;    // query rows [q_row0, q_row0 + q_len) of the q tensor
+  int32_t kv_row0, kv_len;  // key rows [kv_row0, kv_row0 + kv_len) of k/v
+  int64_t delta;            // absolute position of q_row0 minus that of kv_row0
+  int32_t mode;             // PairMode
+  int32_t slot;             // kPartial: workspace slot index
+  int32_t cta_begin;        // filled by the launcher: first block of this pair
+  int32_t n_qtiles;         // filled by the launcher
+};
+
+struct AttnParams {
+  int32_t B, Hq, Hkv, D;
+  int32_t causal, n_pairs;
+  float scale;              // logit scale
+  float scale_log2;         // scale * log2(e)
+  // Raw views of the inputs (the SIMT kernel reads them directly; the tensor
+  // core kernel uses TMA descriptors built from the same views).
+  const void *q, *k, *v;
+  int64_t q_sb, q_ss, q_sh, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh;
+  int64_t q_rows_total, kv_rows_total;  // s extent of the q and k/v tensors
+  int32_t in_f32;           // inputs are fp32 (else bf16)
+  int32_t total_ctas;       // filled by the launcher
+  OutView out;              // final output (absolute q rows)
+  OutView acc;              // Pass-KV fp32 accumulator (absolute q rows)
+  OutView part;             // Pass-Q slot 0 (chunk-relative rows)
+  int64_t part_o_stride;    // elements between slots
+  int64_t part_lse_stride;
+  PairDesc pairs[kMaxPairs];
+};
+
+// N-way merge of Pass-Q partials: for each listed Q chunk, merge `count`
+// consecutive slots starting at `slot0` (ascending KV chunk) into `out`.
+struct MergeNParams {
+  int32_t B, H, D, chunk_rows;
+  int32_t n_items;
+  int32_t pad;
+  OutView out;
+  OutView part;
+  int64_t part_o_stride, part_lse_stride;
+  int32_t item_row0[kMaxPairs];   // absolute first q row of the chunk
+  int32_t item_slot0[kMaxPairs];
+  int32_t item_count[kMaxPairs];  // 0 => empty rows (O = 0, LSE = -inf)
+};
+
+// Pairwise in-place merge.
+struct Merge2Params {
+  int32_t B, S, H, D;
+  OutView a;   // in/out
+  OutView b;
+};
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_attn_tc(AttnParams &p, cudaStream_t stream);
+cudaError_t launch_attn_simt(AttnParams &p, cudaStream_t stream);
+cudaError_t launch_merge_n(const MergeNParams &p, cudaStream_t stream);
+cudaError_t launch_merge_2(const Merge2Params &p, cudaStream_t stream);
+
+// True when the tensor-core kernel supports these shapes.
+bool attn_tc_supported(const AttnParams &p);
+
+// Device status words (one per translation unit that has bounded waits).
+unsigned int attn_tc_read_status(bool clear, cudaError_t *err);
+
+}  // namespace cpattn

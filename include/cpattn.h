@@ -1,0 +1,224 @@
+/*
+ * cpattn.h -- C ABI of libcpattn.so: context-parallel (CP) ring attention for
+ * long-context prefill, single GB300 GPU (sm_103a).
+ *
+ * Source of the operations: "Scaling LLM Inference: Innovations in Tensor
+ * Parallelism, Context Parallelism, and Expert Parallelism" (Meta engineering
+ * article, techreport.ngo rewrite), section "Context Parallelism for
+ * Million-Token Contexts": the sequence is split across CP ranks; in Pass-KV
+ * each rank keeps its Q and exchanges K and V so that it computes attention
+ * over the full context; in Pass-Q the query tensors travel instead.  The
+ * soumitrasaha.com reading notes of the same article (section "The
+ * communication bottleneck across all three axes", CP paragraph) describe the
+ * ring that passes K/V so each rank accumulates the full attention result.
+ * The pages give no formula, interface or kernel; the conventions below are
+ * this library's:
+ *
+ *   - Layout BSHD: q/o are [b, s, hq, d], k/v are [b, s, hkv, d], innermost
+ *     dimension contiguous, other strides given in elements.
+ *   - LSE is fp32, natural log of sum_j exp(scale * q.k_j), laid out
+ *     [b, hq, s] contiguous.  A row with no visible key has LSE = -inf, O = 0.
+ *   - Causal mask: key at absolute position pk is visible to a query at
+ *     absolute position pq iff pk <= pq (inclusive diagonal).
+ *   - GQA: query head h reads kv head h / (hq / hkv).
+ *   - scale <= 0 selects 1/sqrt(d).
+ *
+ * Ownership and concurrency: the caller owns every buffer (inputs, outputs
+ * and workspace are device memory unless stated).  The library never
+ * allocates device memory, never frees, never synchronises the stream it is
+ * given: every compute call only enqueues kernels on `stream` (a
+ * cudaStream_t; NULL = legacy default stream) and returns.
+ *
+ * Errors: argument errors are detected on the host before anything is
+ * enqueued and return CPATTN_ERR_INVALID_ARG / CPATTN_ERR_UNSUPPORTED /
+ * CPATTN_ERR_WORKSPACE with no side effect.  A failed launch returns
+ * CPATTN_ERR_CUDA.  Faults during execution surface at the caller's next
+ * synchronisation.  Kernel-side waits are bounded; one that gives up records
+ * CPATTN_ERR_TIMEOUT in a device status word read by cpattn_device_status().
+ * No C++ exception crosses this interface.
+ */
+#ifndef CPATTN_H_
+#define CPATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CPATTN_OK = 0,
+  CPATTN_ERR_INVALID_ARG = 1,  /* null pointer, bad shape/stride/alignment, bad enum */
+  CPATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head_dim not 64/128) */
+  CPATTN_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or too small */
+  CPATTN_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  CPATTN_ERR_TIMEOUT = 5       /* a kernel-side bounded wait gave up (device status) */
+} cpattn_status;
+
+typedef enum { CPATTN_BF16 = 0, CPATTN_FP32 = 1 } cpattn_dtype;
+
+/* The two ring schedules of the article's CP section. */
+typedef enum { CPATTN_PASS_KV = 1, CPATTN_PASS_Q = 2 } cpattn_mode;
+
+/*
+ * A strided 4-D tensor view [b, s, h, d].  `data` is a device pointer (host
+ * pointer for cpattn_prefill_host), 16-byte aligned.  Strides are in
+ * elements, the d dimension is contiguous, and stride_b/stride_s/stride_h
+ * times the element size must be multiples of 16 bytes.
+ */
+typedef struct {
+  void *data;
+  int32_t dtype; /* cpattn_dtype */
+  int32_t reserved;
+  int64_t b, s, h, d;
+  int64_t stride_b, stride_s, stride_h;
+} cpattn_tensor;
+
+/*
+ * cpattn_partial -- attention of one (Q-chunk, KV-chunk) pair with its LSE.
+ * The per-pair step that both CP schedules run on every rank (article's CP
+ * section, Pass-KV and Pass-Q bullets).
+ *
+ *   q      [b, sq, hq, d]    bf16 or fp32; row i is at absolute position q_off + i
+ *   k, v   [b, skv, hkv, d]  same dtype as q; row j at absolute position kv_off + j
+ *   causal nonzero: mask keys after each query's absolute position
+ *   scale  logit scale; <= 0 selects 1/sqrt(d)
+ *   o      [b, sq, hq, d]    output, bf16 or fp32 (fp32 keeps an unrounded partial)
+ *   lse    [b, hq, sq]       fp32 output, contiguous
+ * d must be 64 or 128; hq % hkv == 0.  sq or skv may be 0 (skv = 0 gives
+ * empty rows: O = 0, LSE = -inf).
+ */
+cpattn_status cpattn_partial(const cpattn_tensor *q, const cpattn_tensor *k,
+                             const cpattn_tensor *v, int64_t q_off, int64_t kv_off,
+                             int causal, float scale, cpattn_tensor *o, float *lse,
+                             void *stream);
+
+/*
+ * cpattn_merge -- in place, (o_a, lse_a) <- merge((o_a, lse_a), (o_b, lse_b)),
+ * the LSE-weighted combination of two partial results over disjoint key sets:
+ *   LSE = log(exp(LSE_a) + exp(LSE_b)),
+ *   O   = exp(LSE_a - LSE) O_a + exp(LSE_b - LSE) O_b.
+ * This is how a rank folds another rank's contribution into its own so that
+ * it "accumulates the full attention result" (reading notes, CP paragraph).
+ * o_a and o_b: same shape [b, s, h, d], same dtype (bf16 or fp32); lse_a and
+ * lse_b: [b, h, s] fp32 contiguous.  Both sides -inf gives (0, -inf).
+ */
+cpattn_status cpattn_merge(cpattn_tensor *o_a, float *lse_a, const cpattn_tensor *o_b,
+                           const float *lse_b, void *stream);
+
+/*
+ * cpattn_prefill_workspace_size -- device bytes cpattn_prefill needs for the
+ * given shapes, schedule and mask.  Pass-KV: an fp32 running accumulator
+ * [b, sq, hq, d] plus its LSE.  Pass-Q: one fp32 partial (O and LSE) per
+ * non-empty (Q-chunk, KV-chunk) pair of every Q chunk that more than one KV
+ * chunk reaches.  Writes the size to *bytes (0 is possible).
+ */
+cpattn_status cpattn_prefill_workspace_size(const cpattn_tensor *q, const cpattn_tensor *k,
+                                            int64_t q_base, int n_chunks, int mode,
+                                            int causal, size_t *bytes);
+
+/*
+ * cpattn_prefill -- CP prefill of one attention layer, emulating n_chunks CP
+ * ranks on one GPU (article's CP section).  Q rows [c*sq/N, (c+1)*sq/N) and
+ * K/V rows [c*skv/N, (c+1)*skv/N) form chunk c; query row i is at absolute
+ * position q_base + i and key row j at position j.  Ring step t pairs rank r
+ * with chunk (r - t) mod N of the travelling tensor: K/V for CPATTN_PASS_KV
+ * (Q resident, online LSE accumulation fused into the attention kernel's
+ * epilogue), Q for CPATTN_PASS_Q (K/V resident, per-pair partials merged by
+ * LSE in ascending KV-chunk order after the ring).  Pairs with no visible key
+ * are skipped.  Steps are launched back to back on `stream`.
+ *
+ *   n_chunks  1..64, dividing both sq and skv
+ *   o         [b, sq, hq, d] bf16 or fp32;  lse [b, hq, sq] fp32 contiguous
+ *   workspace device buffer of at least cpattn_prefill_workspace_size bytes,
+ *             256-byte aligned (may be NULL when that size is 0)
+ * Result: full causal attention of every query row over keys 0..skv-1.
+ */
+cpattn_status cpattn_prefill(const cpattn_tensor *q, const cpattn_tensor *k,
+                             const cpattn_tensor *v, int64_t q_base, int n_chunks,
+                             int mode, int causal, float scale, cpattn_tensor *o,
+                             float *lse, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/*
+ * One entry of the host-side ring plan (no GPU needed): at ring `step`, the
+ * pair (q_chunk, kv_chunk) is computed and its result routed by `role`.
+ */
+typedef enum {
+  CPATTN_ROLE_STORE = 0,      /* only contribution: write O/LSE to the output */
+  CPATTN_ROLE_ACC_INIT = 1,   /* Pass-KV: first contribution, start the accumulator */
+  CPATTN_ROLE_ACC_MERGE = 2,  /* Pass-KV: merge into the accumulator */
+  CPATTN_ROLE_ACC_FINAL = 3,  /* Pass-KV: last contribution, merge and write the output */
+  CPATTN_ROLE_PARTIAL = 4     /* Pass-Q: write an fp32 partial to workspace slot `slot` */
+} cpattn_role;
+
+typedef struct {
+  int32_t step, q_chunk, kv_chunk, role, slot;
+} cpattn_plan_entry;
+
+/*
+ * cpattn_prefill_plan -- the pair list cpattn_prefill launches, in launch
+ * order (host computation only).  Writes up to `capacity` entries and the
+ * total count to *n_entries; returns CPATTN_ERR_INVALID_ARG for bad sizes.
+ */
+cpattn_status cpattn_prefill_plan(int64_t sq, int64_t skv, int64_t q_base, int n_chunks,
+                                  int mode, int causal, cpattn_plan_entry *entries,
+                                  int capacity, int *n_entries);
+
+/*
+ * cpattn_prefill_host -- end-to-end convenience: q, k, v, o are HOST tensors
+ * (pageable or pinned); lse is a host array [b, hq, sq].  Copies inputs to
+ * device staging buffers the caller provides (`dev_scratch`, at least
+ * cpattn_prefill_host_scratch_size bytes, 256-byte aligned), runs
+ * cpattn_prefill there, copies O and LSE back, and synchronises `stream`.
+ */
+cpattn_status cpattn_prefill_host_scratch_size(const cpattn_tensor *q, const cpattn_tensor *k,
+                                               int64_t q_base, int n_chunks, int mode,
+                                               int causal, int out_dtype, size_t *bytes);
+cpattn_status cpattn_prefill_host(const cpattn_tensor *q, const cpattn_tensor *k,
+                                  const cpattn_tensor *v, int64_t q_base, int n_chunks,
+                                  int mode, int causal, float scale, cpattn_tensor *o,
+                                  float *lse, void *dev_scratch, size_t scratch_bytes,
+                                  void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *cpattn_status_string(cpattn_status s);
+
+/*
+ * cpattn_device_status -- read (and if `clear`, reset) the device status word
+ * that kernels set when a bounded wait gives up.  Synchronises the device.
+ * Returns CPATTN_OK, CPATTN_ERR_TIMEOUT or CPATTN_ERR_CUDA.
+ */
+cpattn_status cpattn_device_status(int clear);
+
+/*
+ * Launch profiling for benchmarks.  cpattn_profile_begin(capacity) arms
+ * recording: each later kernel launch by this library records a pair of CUDA
+ * events around it on its stream (host-side resources only, up to
+ * `capacity` launches).  cpattn_profile_end() synchronises those events,
+ * fills up to `capacity` records and disarms.  `work` is the launch's
+ * algorithmic work: causal-effective FLOPs for attention kernels, bytes
+ * moved for merge kernels.  Not thread safe.
+ */
+typedef enum {
+  CPATTN_KERNEL_ATTN_TC = 1,    /* tcgen05 partial-attention kernel */
+  CPATTN_KERNEL_ATTN_SIMT = 2,  /* fp32 / head_dim 64 partial-attention kernel */
+  CPATTN_KERNEL_MERGE2 = 3,     /* pairwise LSE merge */
+  CPATTN_KERNEL_MERGEN = 4      /* N-way LSE merge of Pass-Q partials */
+} cpattn_kernel_kind;
+
+typedef struct {
+  int32_t kind; /* cpattn_kernel_kind */
+  float ms;
+  double work;
+} cpattn_profile_record;
+
+cpattn_status cpattn_profile_begin(int capacity);
+cpattn_status cpattn_profile_end(cpattn_profile_record *records, int capacity, int *n_records);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H_ */

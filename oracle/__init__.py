@@ -35,13 +35,13 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (-O2, OpenMP).  Returns the .so path."""
+    """Compile the oracle with gcc (-O3, OpenMP).  Returns the .so path."""
     os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC,
+    cmd = ["gcc", "-O3", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC,
            "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)

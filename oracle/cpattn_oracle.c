@@ -105,6 +105,7 @@ int cpattn_oracle_attention(const float *q, const int64_t *q_pos, int64_t nq,
       for (int64_t j = 0; j < n_vis; ++j) {
         const float *kj = k + ((b * Skv + j) * Hkv + hk) * D;
         double dot = 0.0;
+#pragma omp simd reduction(+ : dot)
         for (int64_t t = 0; t < D; ++t) dot += (double)qi[t] * (double)kj[t];
         s[j] = scale * dot;
         if (s[j] > m) m = s[j];

@@ -1,0 +1,216 @@
+"""Host-side checks of libcpattn.so that need no GPU: the library loads, it
+exports every function include/cpattn.h declares, argument errors come back
+as status codes before any CUDA call, and the ring plan -- driven through the
+fp64 oracle on the CPU -- reproduces unchunked causal attention."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from context_ring_attention_cpattn_gb300 import binding as B
+from context_ring_attention_cpattn_gb300 import build as pkg_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cpattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkg_build.build()
+    return B.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cpattn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(B.EXPORTED)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def T(data=0x10000, dtype=B.BF16, b=1, s=256, h=4, d=128, stride=None):
+    if stride is None:
+        stride = (s * h * d, h * d, d)
+    return B.CpattnTensor(data, dtype, 0, b, s, h, d, *stride)
+
+
+def call_partial(lib, q, k, v, o, lse=0x20000, q_off=0, kv_off=0):
+    return lib.cpattn_partial(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), q_off, kv_off, 1,
+                              0.0, ctypes.byref(o), lse, None)
+
+
+INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 3
+
+
+@pytest.mark.parametrize("case,expect", [
+    ("null_q", INVALID), ("bad_dtype", INVALID), ("mixed_dtype", INVALID), ("gqa_indivisible", INVALID),
+    ("head_dim_96", UNSUPPORTED), ("misaligned_ptr", INVALID), ("misaligned_stride", INVALID),
+    ("kv_len_mismatch", INVALID), ("out_shape", INVALID), ("null_lse", INVALID),
+    ("null_data", INVALID), ("batch_mismatch", INVALID)])
+def test_partial_argument_errors(lib, case, expect):
+    q, k, v, o = T(h=8), T(h=2), T(h=2), T(h=8)
+    lse = 0x20000
+    if case == "null_q":
+        assert lib.cpattn_partial(None, ctypes.byref(k), ctypes.byref(v), 0, 0, 1, 0.0,
+                                  ctypes.byref(o), lse, None) == expect
+        return
+    if case == "bad_dtype":
+        q.dtype = 7
+    elif case == "mixed_dtype":
+        k.dtype = B.FP32
+    elif case == "gqa_indivisible":
+        q.h, o.h = 6, 6
+        k.h, v.h = 4, 4
+    elif case == "head_dim_96":
+        for t in (q, k, v, o):
+            t.d = 96
+    elif case == "misaligned_ptr":
+        q.data = 0x10008
+    elif case == "misaligned_stride":
+        k.stride_s = 2 * 128 + 4
+    elif case == "kv_len_mismatch":
+        v.s = 128
+    elif case == "out_shape":
+        o.s = 255
+    elif case == "null_lse":
+        lse = None
+    elif case == "null_data":
+        q.data = None
+    elif case == "batch_mismatch":
+        k.b = 2
+    assert call_partial(lib, q, k, v, o, lse) == expect
+
+
+def test_prefill_argument_errors(lib):
+    q, k, v, o = T(h=8, s=1024), T(h=1, s=1024), T(h=1, s=1024), T(h=8, s=1024)
+    size = ctypes.c_size_t()
+    # n_chunks must divide both lengths, lie in 1..64; mode must be 1 or 2.
+    for n, mode in ((3, 1), (0, 1), (65, 1), (4, 3)):
+        assert lib.cpattn_prefill_workspace_size(ctypes.byref(q), ctypes.byref(k), 0, n, mode, 1,
+                                                 ctypes.byref(size)) == INVALID
+    assert lib.cpattn_prefill_workspace_size(ctypes.byref(q), ctypes.byref(k), 0, 4, 1, 1,
+                                             ctypes.byref(size)) == 0
+    need = size.value
+    assert need == 1024 * 8 * 128 * 4 + 1024 * 8 * 4
+    # Missing / short / misaligned workspace is rejected before any launch.
+    args = lambda ws, n: (ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), 0, 4, 1, 1, 0.0,
+                          ctypes.byref(o), 0x20000, ws, n, None)
+    assert lib.cpattn_prefill(*args(None, 0)) == WORKSPACE
+    assert lib.cpattn_prefill(*args(0x40000, need - 1)) == WORKSPACE
+    assert lib.cpattn_prefill(*args(0x40010, need)) == WORKSPACE
+
+
+def test_workspace_sizes(lib):
+    # Pass-Q keeps one fp32 partial per visible pair of chunks reached more than once.
+    q, k = T(h=16, s=4096), T(h=1, s=4096)
+    size = ctypes.c_size_t()
+    assert lib.cpattn_prefill_workspace_size(ctypes.byref(q), ctypes.byref(k), 0, 4, 2, 1,
+                                             ctypes.byref(size)) == 0
+    slots = 2 + 3 + 4   # chunks 1..3 reach 2, 3, 4 KV chunks; chunk 0 reaches one
+    per_slot_o, per_slot_l = 1024 * 16 * 128 * 4, 16 * 1024 * 4
+    align = lambda x: (x + 255) // 256 * 256
+    assert size.value == align(slots * per_slot_o) + align(slots * per_slot_l)
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.cpattn_status_string(code).decode().startswith("CPATTN")
+
+
+# --------------------------------------------------------------------- the ring plan
+def plan_cases():
+    return [(256, 256, 0, 4, True), (256, 256, 0, 4, False), (2048, 32768, 30720, 8, True),
+            (96, 192, 40, 3, True), (64, 64, 0, 1, True), (120, 120, -50, 5, True),
+            (64, 64, 500, 8, True)]
+
+
+@pytest.mark.parametrize("sq,skv,q_base,n,causal", plan_cases())
+@pytest.mark.parametrize("mode", [B.PASS_KV, B.PASS_Q])
+def test_plan_structure(lib, sq, skv, q_base, n, causal, mode):
+    plan = B.prefill_plan(sq, skv, n, mode, q_base, causal)
+    cq, c = sq // n, skv // n
+    visible = {(i, j) for i in range(n) for j in range(n)
+               if (not causal) or j * c <= q_base + i * cq + cq - 1}
+    assert sorted((e[1], e[2]) for e in plan) == sorted(visible)
+    steps = [e[0] for e in plan]
+    assert steps == sorted(steps)
+    for step, i, j, role, slot in plan:
+        if mode == B.PASS_KV:
+            assert j == (i - step) % n      # rank i holds Q chunk i, K/V travel
+        else:
+            assert i == (j - step) % n      # rank j holds K/V chunk j, Q travel
+    for t in set(steps):
+        ranks = [e[1] if mode == B.PASS_KV else e[2] for e in plan if e[0] == t]
+        assert len(ranks) == len(set(ranks))  # one pair per rank per step
+    slots = [e[4] for e in plan if e[3] == 4]
+    assert len(slots) == len(set(slots))
+
+
+def emulate_plan(q, k, v, n, mode, q_base, causal):
+    """Run the library's plan on the CPU with oracle partials and merges."""
+    Bsz, sq, hq, d = q.shape
+    skv = k.shape[1]
+    cq, c = sq // n, skv // n
+    plan = B.prefill_plan(sq, skv, n, mode, q_base, causal)
+    out_o = np.full((Bsz, sq, hq, d), np.nan)
+    out_l = np.full((Bsz, hq, sq), np.nan)
+    acc = {}
+    slots = {}
+    for step, i, j, role, slot in plan:
+        o, lse = oracle.attention(q[:, i * cq:(i + 1) * cq], k[:, j * c:(j + 1) * c],
+                                  v[:, j * c:(j + 1) * c],
+                                  q_pos=q_base + np.arange(i * cq, (i + 1) * cq), kv_pos0=j * c,
+                                  causal=causal)
+        lse_t = np.transpose(lse, (0, 2, 1))
+        name = B.ROLE_NAMES[role]
+        if name == "store":
+            out_o[:, i * cq:(i + 1) * cq], out_l[:, :, i * cq:(i + 1) * cq] = o, lse
+        elif name == "acc_init":
+            acc[i] = (o, lse_t)
+        elif name in ("acc_merge", "acc_final"):
+            mo, ml = oracle.merge(np.stack([acc[i][0], o]), np.stack([acc[i][1], lse_t]))
+            acc[i] = (mo, ml)
+            if name == "acc_final":
+                out_o[:, i * cq:(i + 1) * cq] = mo
+                out_l[:, :, i * cq:(i + 1) * cq] = np.transpose(ml, (0, 2, 1))
+        else:
+            slots[slot] = (i, j, o, lse_t)
+    for i in range(n):
+        parts = sorted((s, val) for s, val in slots.items() if val[0] == i)
+        if parts:
+            assert [val[1] for _, val in parts] == sorted(val[1] for _, val in parts)
+            mo, ml = oracle.merge(np.stack([val[2] for _, val in parts]),
+                                  np.stack([val[3] for _, val in parts]))
+            out_o[:, i * cq:(i + 1) * cq] = mo
+            out_l[:, :, i * cq:(i + 1) * cq] = np.transpose(ml, (0, 2, 1))
+        elif np.isnan(out_l[:, :, i * cq:(i + 1) * cq]).all():
+            out_o[:, i * cq:(i + 1) * cq] = 0.0         # no key reaches this chunk
+            out_l[:, :, i * cq:(i + 1) * cq] = -np.inf
+    return out_o, out_l
+
+
+@pytest.mark.parametrize("sq,skv,q_base,n,causal", plan_cases())
+@pytest.mark.parametrize("mode", [B.PASS_KV, B.PASS_Q])
+def test_plan_reproduces_full_attention(lib, sq, skv, q_base, n, causal, mode):
+    if skv > 4096:
+        sq, skv, q_base = sq // 16, skv // 16, q_base // 16
+    rng = np.random.default_rng(sq + skv + n)
+    q = rng.standard_normal((1, sq, 2, 8)).astype(np.float32)
+    k = rng.standard_normal((1, skv, 1, 8)).astype(np.float32)
+    v = rng.standard_normal((1, skv, 1, 8)).astype(np.float32)
+    o, lse = emulate_plan(q, k, v, n, mode, q_base, causal)
+    ref_o, ref_l = oracle.attention(q, k, v, q_pos=q_base + np.arange(sq), causal=causal)
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+    assert np.array_equal(np.isneginf(lse), np.isneginf(ref_l))
+    fin = np.isfinite(ref_l)
+    np.testing.assert_allclose(lse[fin], ref_l[fin], rtol=0, atol=1e-12)

@@ -1,0 +1,94 @@
+"""CP prefill (Pass-KV and Pass-Q) on the five long-context workloads against
+the fp64 oracle: every row for the small ones, a seeded sample of query rows
+(first and last row of every chunk included) for the large ones.  Pass-KV and
+Pass-Q must also agree with each other on every element, and each schedule
+must be bitwise reproducible."""
+import os
+
+import numpy as np
+import pytest
+
+from tests.gpu_util import TOL, compare, oracle_rows
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+N_SAMPLE = int(os.environ.get("CPATTN_SAMPLE_ROWS", "4096"))
+
+
+@pytest.fixture(scope="module")
+def B():
+    from context_ring_attention_cpattn_gb300 import binding, build
+
+    build.build()
+    return binding
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3-8b", "partial-32k", "128k", "1m"])
+def test_prefill_workload(B, name):
+    from context_ring_attention_cpattn_gb300.workloads import WORKLOADS, make_qkv, sample_rows
+
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w, device="cuda")
+    tol = TOL[w.dtype]
+    outs = {}
+    for mode in (B.PASS_KV, B.PASS_Q):
+        o, lse = B.prefill(q, k, v, w.n_chunks, mode, q_base=w.q_base, causal=w.causal)
+        torch.cuda.synchronize()
+        assert B.device_status() == 0
+        outs[mode] = (o, lse)
+    rows = sample_rows(w, n=min(N_SAMPLE, w.sq))
+    ref_o, ref_l = oracle_rows(q, k, v, rows, q_base=w.q_base, causal=w.causal)
+    for mode, (o, lse) in outs.items():
+        compare(o, lse, rows, ref_o, ref_l, tol, f"{name} mode {mode}")
+    # Pass-KV and Pass-Q agree on every element.
+    (o1, l1), (o2, l2) = outs[B.PASS_KV], outs[B.PASS_Q]
+    d_o = (o1.float() - o2.float()).abs().max().item()
+    d_l = (l1 - l2).abs().max().item()
+    assert d_o <= tol[0] and d_l <= tol[1], (d_o, d_l)
+    # Bitwise reproducible: no atomics, fixed merge order.
+    for mode in (B.PASS_KV, B.PASS_Q):
+        o, lse = B.prefill(q, k, v, w.n_chunks, mode, q_base=w.q_base, causal=w.causal)
+        torch.cuda.synchronize()
+        assert torch.equal(o, outs[mode][0]) and torch.equal(lse, outs[mode][1])
+    del outs, q, k, v
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("case", [
+    # (sq, skv, hq, hkv, n_chunks, q_base, dtype)
+    (1000, 1000, 4, 2, 8, 0, "bf16"),       # chunks of 125 rows: ragged tiles everywhere
+    (384, 768, 4, 1, 3, 384, "bf16"),       # more keys than queries, partial prefill
+    (192, 192, 2, 1, 6, -64, "bf16"),       # first chunks see no key at all
+    (240, 240, 2, 2, 5, 0, "fp32"),         # fp32 path, hq == hkv
+])
+def test_prefill_edge_cases(B, case, mode):
+    sq, skv, hq, hkv, n, q_base, dt = case
+    dtype = torch.bfloat16 if dt == "bf16" else torch.float32
+    g = torch.Generator(device="cuda")
+    g.manual_seed(sq + skv + n)
+    q = torch.randn((1, sq, hq, 128), generator=g, device="cuda").to(dtype)
+    k = torch.randn((1, skv, hkv, 128), generator=g, device="cuda").to(dtype)
+    v = torch.randn((1, skv, hkv, 128), generator=g, device="cuda").to(dtype)
+    o, lse = B.prefill(q, k, v, n, mode, q_base=q_base)
+    torch.cuda.synchronize()
+    rows = np.arange(sq)
+    ref_o, ref_l = oracle_rows(q, k, v, rows, q_base=q_base)
+    compare(o, lse, rows, ref_o, ref_l, TOL[dt], f"edge {case} mode {mode}")
+
+
+def test_prefill_host_entry_point(B):
+    """The host-buffer entry point gives the same result as the device one."""
+    from context_ring_attention_cpattn_gb300.workloads import WORKLOADS, make_qkv
+
+    w = WORKLOADS["llama3-8b"]
+    q, k, v = make_qkv(w, device="cuda")
+    o_ref, l_ref = B.prefill(q, k, v, w.n_chunks, B.PASS_KV)
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = torch.empty_like(qh).pin_memory()
+    lh = torch.empty((1, w.hq, w.sq), dtype=torch.float32).pin_memory()
+    scratch = torch.empty(B.host_scratch_size(qh, kh, w.n_chunks, B.PASS_KV), dtype=torch.uint8,
+                          device="cuda")
+    B.prefill_host(qh, kh, vh, w.n_chunks, B.PASS_KV, oh, lh, scratch)
+    assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())
