@@ -219,12 +219,11 @@ def run_reference(args, w):
 
 
 # ----------------------------------------------------------------- GPU arm
-def time_modes(B, w, q, k, v, outs, wss, steps, warmup, world, profile_cap=0):
-    """Warm up, then time `steps` steps of (Pass-KV, Pass-Q).  Returns the
-    elapsed ms (max over ranks), per-mode ms lists and profile records."""
+def time_modes(B, w, q, k, v, outs, wss, steps, warmup, world, modes, profile_cap=0):
+    """Warm up, then time `steps` steps, each running the given schedules in
+    order.  Returns the elapsed ms (max over ranks), per-schedule ms lists and
+    profile records."""
     import torch
-
-    modes = (B.PASS_KV, B.PASS_Q)
 
     def one(mode):
         o, lse = outs[mode]
@@ -261,11 +260,11 @@ def time_modes(B, w, q, k, v, outs, wss, steps, warmup, world, profile_cap=0):
     return max_over_ranks(elapsed, world), per_mode, recs
 
 
-def make_buffers(B, w, q, k):
+def make_buffers(B, w, q, k, modes):
     import torch
 
     outs, wss = {}, {}
-    for mode in (B.PASS_KV, B.PASS_Q):
+    for mode in modes:
         outs[mode] = (torch.empty_like(q),
                       torch.empty((w.batch, w.hq, w.sq), dtype=torch.float32, device=q.device))
         n = B.workspace_size(q, k, w.n_chunks, mode, w.q_base, w.causal)
@@ -282,8 +281,11 @@ def main():
     ap.add_argument("--workload", default="128k")
     ap.add_argument("--skip-1m", action="store_true", help="do not time the 1M-token layer")
     ap.add_argument("--skip-e2e", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=96, help="oracle rows for cpu_baseline")
-    ap.add_argument("--ref-rows", type=int, default=16, help="oracle rows per reference step")
+    ap.add_argument("--schedules", default="both", choices=["both", "kv", "q"],
+                    help="ring schedules in one step (default: Pass-KV then Pass-Q)")
+    ap.add_argument("--cpu-rows", type=int, default=2048,
+                    help="oracle rows for cpu_baseline (0 skips it)")
+    ap.add_argument("--ref-rows", type=int, default=256, help="oracle rows per reference step")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: warmup raised to 3 (timing rule)", file=sys.stderr)
@@ -307,12 +309,14 @@ def main():
     barrier(world)
     B.lib()
 
+    modes = {"both": (B.PASS_KV, B.PASS_Q), "kv": (B.PASS_KV,), "q": (B.PASS_Q,)}[args.schedules]
+    names = {B.PASS_KV: "pass_kv", B.PASS_Q: "pass_q"}
     q, k, v = make_qkv(w, device="cuda")
-    outs, wss = make_buffers(B, w, q, k)
+    outs, wss = make_buffers(B, w, q, k, modes)
     flops_layer = w.causal_flops()
-    flops_step = 2 * flops_layer
+    flops_step = len(modes) * flops_layer
     launches_per_step = 0
-    for mode in (B.PASS_KV, B.PASS_Q):
+    for mode in modes:
         plan = B.prefill_plan(w.sq, w.skv, w.n_chunks, mode, w.q_base, w.causal)
         launches_per_step += len({e[0] for e in plan}) + 1
     cap = (launches_per_step + 4) * args.steps
@@ -320,7 +324,7 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     elapsed, per_mode, recs = time_modes(B, w, q, k, v, outs, wss, args.steps, args.warmup, world,
-                                         profile_cap=cap)
+                                         modes, profile_cap=cap)
     clk = clocks.stop()
     ms_step = elapsed / args.steps
     value = world * flops_step * args.steps / (elapsed * 1e-3) / 1e12
@@ -341,11 +345,11 @@ def main():
                 "launches_timed": len(tc), "avg_launch_ms": tc_ms / len(tc) if tc else None,
                 "share_of_step": tc_ms / elapsed if elapsed else None}
 
-    ms_layer = {"pass_kv": statistics.median(per_mode[B.PASS_KV]),
-                "pass_q": statistics.median(per_mode[B.PASS_Q])}
+    ms_layer = {names[m]: statistics.median(per_mode[m]) for m in modes}
     cfg = {"workload": w.name, "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim,
            "seq_len": w.sq, "n_chunks": w.n_chunks, "causal": w.causal,
-           "step": "Pass-KV prefill + Pass-Q prefill of one layer",
+           "step": " + ".join({"pass_kv": "Pass-KV prefill", "pass_q": "Pass-Q prefill"}[names[m]]
+                               for m in modes) + " of one layer",
            "flops_per_layer": flops_layer, "ms_per_layer": ms_layer,
            "tflops_per_schedule": {k_: flops_layer / (v_ * 1e-3) / 1e12 for k_, v_ in ms_layer.items()},
            "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
@@ -359,17 +363,17 @@ def main():
         torch.cuda.empty_cache()
         w1 = WORKLOADS["1m"]
         q1, k1, v1 = make_qkv(w1, device="cuda")
-        outs1, wss1 = make_buffers(B, w1, q1, k1)
+        outs1, wss1 = make_buffers(B, w1, q1, k1, modes)
         steps1 = max(1, args.steps // 5)
-        _, pm1, _ = time_modes(B, w1, q1, k1, v1, outs1, wss1, steps1, 1, world)
-        ms1 = {"pass_kv": statistics.median(pm1[B.PASS_KV]), "pass_q": statistics.median(pm1[B.PASS_Q])}
+        _, pm1, _ = time_modes(B, w1, q1, k1, v1, outs1, wss1, steps1, 1, world, modes)
+        ms1 = {names[m]: statistics.median(pm1[m]) for m in modes}
         f1 = w1.causal_flops()
         cfg["ms_per_layer_1m"] = ms1
         cfg["tflops_per_schedule_1m"] = {k_: f1 / (v_ * 1e-3) / 1e12 for k_, v_ in ms1.items()}
         cfg["steps_1m"] = steps1
         del outs1, wss1, q1, k1, v1
         torch.cuda.empty_cache()
-        outs, wss = make_buffers(B, w, q, k)
+        outs, wss = make_buffers(B, w, q, k, modes)
 
     # ---- end to end through the host-buffer entry point
     e2e = None
@@ -378,13 +382,13 @@ def main():
         oh = torch.empty_like(qh).pin_memory()
         lh = torch.empty((w.batch, w.hq, w.sq), dtype=torch.float32).pin_memory()
         need = max(B.host_scratch_size(qh, kh, w.n_chunks, m, w.q_base, w.causal)
-                   for m in (B.PASS_KV, B.PASS_Q))
+                   for m in modes)
         del outs, wss
         torch.cuda.empty_cache()
         scratch = torch.empty(need, dtype=torch.uint8, device="cuda")
 
         def host_step():
-            for m in (B.PASS_KV, B.PASS_Q):
+            for m in modes:
                 B.prefill_host(qh, kh, vh, w.n_chunks, m, oh, lh, scratch, q_base=w.q_base,
                                causal=w.causal)
 
@@ -398,14 +402,15 @@ def main():
         in_bytes = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
         out_bytes = oh.numel() * oh.element_size() + lh.numel() * 4
         e2e = {"value": world * flops_step * args.steps / t_e2e / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": 2 * in_bytes, "d2h_bytes_per_step": 2 * out_bytes,
+               "h2d_bytes_per_step": len(modes) * in_bytes,
+               "d2h_bytes_per_step": len(modes) * out_bytes,
                "ms_per_step": 1e3 * t_e2e / args.steps,
                "path": "cpattn_prefill_host (pinned host buffers; copies inside the timed region)"}
         del scratch
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0 only)
     cpu_baseline = None
-    if rank == 0:
+    if rank == 0 and args.cpu_rows > 0:
         f, dt, threads, rows = oracle_sample(w, args.cpu_rows)
         cpu_baseline = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                         "sample": f"{args.cpu_rows} seeded query rows x {w.hq} heads of the {w.name} "

@@ -7,7 +7,8 @@
 //   kAccMerge  acc  <- merge(acc, (O_p, LSE_p))           (Pass-KV, middle steps)
 //   kAccFinal  out  <- merge(acc, (O_p, LSE_p))           (Pass-KV, last step)
 //
-// merge((O_a, L_a), (O_b, L_b)) = (w_a O_a + w_b O_b, L) with
+// merge((O_a, L_a), (O_b, L_b)) = (w_a O_a + w_b O_b, L) (products rounded
+// separately, so the merge is bitwise symmetric in its two sides) with
 // L = log(e^{L_a} + e^{L_b}), w = e^{L_x - L}: the LSE-weighted combination of
 // partials over disjoint key sets that lets a CP rank accumulate the full
 // attention result as K/V chunks arrive around the ring ("Scaling LLM
@@ -108,7 +109,6 @@ struct RowSink {
   int dst_f32;
   const float *acc;  // accumulator row read by the merge roles
   float wa, wb;    // merge weights (merge roles)
-  float scale_p;   // weight applied to the partial (1 for plain stores)
 
   // rel_row: row inside the pair's q chunk.  lse_p: the partial's LSE.
   // write_lse: this thread writes the LSE (one thread per row and head).
@@ -119,7 +119,6 @@ struct RowSink {
     acc = nullptr;
     wa = 0.f;
     wb = 1.f;
-    scale_p = 1.f;
     if (mode == kStore) {
       dst = view_row(p.out, b, abs_row, h);
       dst_f32 = p.out.f32;
@@ -141,7 +140,6 @@ struct RowSink {
       const MergeW mw = merge_weights(*acc_lse, lse_p);
       wa = mw.wa;
       wb = mw.wb;
-      scale_p = mw.wb;
       if (mode == kAccMerge) {
         dst = const_cast<float *>(acc);
         dst_f32 = 1;
@@ -161,7 +159,7 @@ struct RowSink {
       float a[N];
       load_f32<N>(acc, c0, a);
 #pragma unroll
-      for (int i = 0; i < N; ++i) v[i] = wa * a[i] + wb * v[i];
+      for (int i = 0; i < N; ++i) v[i] = __fmul_rn(wa, a[i]) + __fmul_rn(wb, v[i]);
     }
     store_vals<N>(dst, dst_f32, c0, v);
   }

@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kWarps * 32) merge2_kernel(const __grid_consta
     load_row<E>(p.a, b, s, h, lane * E, va);
     load_row<E>(p.b, b, s, h, lane * E, vb);
 #pragma unroll
-    for (int i = 0; i < E; ++i) va[i] = w.wa * va[i] + w.wb * vb[i];
+    for (int i = 0; i < E; ++i) va[i] = __fmul_rn(w.wa, va[i]) + __fmul_rn(w.wb, vb[i]);
     __syncwarp();
     store_vals<E>(view_row(p.a, b, s, h), p.a.f32, lane * E, va);
     if (lane == 0) *la = w.lse;
