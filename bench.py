@@ -35,10 +35,11 @@ sys.path.insert(0, ROOT)
 METRIC = "CP prefill causal TFLOP/s & % of GB300 BF16 peak; ms/layer at 128K and 1M tokens"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
-# DRAM bytes (read + write) per launch of the tensor-core attention kernel
-# from one ncu capture, and the kernel source it was taken from.  Set to None
-# until a capture of the current source exists.
-TRAFFIC_RECORD = None  # {"sha": "...", "bytes_per_flop": float, "capture": "..."}
+# DRAM bytes (read + write) per tensor FLOP of the tensor-core attention
+# kernel from one ncu capture, and the kernel source it was taken from; the
+# roofline's traffic is null whenever the source differs from the capture.
+TRAFFIC_RECORD = {"sha": "0930d60a5f646cda", "bytes_per_flop": 3.036e-4,
+                  "capture": "profiles/attn_tc_128k_passkv_step2.md"}
 
 
 def load_peaks():
