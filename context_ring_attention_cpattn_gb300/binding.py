@@ -37,8 +37,8 @@ class ProfileRecord(ctypes.Structure):
 
 EXPORTED = ["cpattn_partial", "cpattn_merge", "cpattn_prefill_workspace_size", "cpattn_prefill",
             "cpattn_prefill_plan", "cpattn_prefill_host_scratch_size", "cpattn_prefill_host",
-            "cpattn_status_string", "cpattn_device_status", "cpattn_profile_begin",
-            "cpattn_profile_end"]
+            "cpattn_prefill_noalloc", "cpattn_status_string", "cpattn_device_status",
+            "cpattn_profile_begin", "cpattn_profile_end"]
 
 _lib = None
 
@@ -75,6 +75,7 @@ def lib():
     L.cpattn_prefill_host_scratch_size.argtypes = [T, T, i64, i32, i32, i32, i32, sz]
     L.cpattn_prefill_host.argtypes = [T, T, T, i64, i32, i32, i32, f32, T, vp, vp, ctypes.c_size_t,
                                       vp]
+    L.cpattn_prefill_noalloc.argtypes = [T, T, T, i64, i32, i32, i32, f32, T, vp, vp]
     L.cpattn_status_string.argtypes = [i32]
     L.cpattn_status_string.restype = ctypes.c_char_p
     L.cpattn_device_status.argtypes = [i32]
@@ -175,6 +176,25 @@ def prefill(q, k, v, n_chunks: int, mode: int, q_base: int = 0, causal: bool = T
                                 int(q_base), int(n_chunks), int(mode), int(bool(causal)),
                                 float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(), ws_ptr,
                                 ws_len, _stream(stream)), "cpattn_prefill")
+    return out, lse
+
+
+def prefill_noalloc(q, k, v, n_chunks: int, mode: int, q_base: int = 0, causal: bool = True,
+                    scale=None, out=None, lse=None, stream=None):
+    """cpattn_prefill with the library's static workspace (no allocation by
+    the library); see cpattn_prefill_noalloc."""
+    import torch
+
+    B, S, H, D = q.shape
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    qv, kv_, vv, ov = view(q), view(k), view(v), view(out)
+    _check(lib().cpattn_prefill_noalloc(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
+                                        int(q_base), int(n_chunks), int(mode), int(bool(causal)),
+                                        float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(),
+                                        _stream(stream)), "cpattn_prefill_noalloc")
     return out, lse
 
 

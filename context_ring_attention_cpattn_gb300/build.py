@@ -14,7 +14,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libcpattn.so")
-SOURCES = ["api.cu", "attn_tc.cu", "attn_simt.cu", "merge.cu"]
+SOURCES = ["api.cu", "attn_tc.cu", "attn_simt.cu", "merge.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]

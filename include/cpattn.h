@@ -182,6 +182,37 @@ cpattn_status cpattn_prefill_host(const cpattn_tensor *q, const cpattn_tensor *k
                                   float *lse, void *dev_scratch, size_t scratch_bytes,
                                   void *stream);
 
+/*
+ * cpattn_prefill_noalloc -- cpattn_prefill without a caller-provided
+ * workspace; this call allocates nothing.  The paper has no counterpart: it
+ * is an interface convenience of this library.
+ *
+ * For callers that cannot call cudaMalloc: code embedded in a framework whose
+ * own pool owns all device memory and forbids raw allocations, or a
+ * latency-critical loop that cannot afford cudaMalloc's implicit device
+ * synchronisation.  The caller still provides q, k, v, o and lse; the Pass-KV
+ * accumulator or the Pass-Q partial stack lives in one static device buffer
+ * of CPATTN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads this code holds until the process exits.
+ *
+ *   - Problems whose cpattn_prefill_workspace_size exceeds
+ *     CPATTN_NOALLOC_SCRATCH_BYTES return CPATTN_ERR_UNSUPPORTED before
+ *     anything is enqueued (e.g. Pass-KV fits sq * hq * b <= ~130K rows at d = 128).
+ *   - The first call on a device looks up the buffer's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one buffer and it keeps the previous call's
+ *     contents; nothing in it has to start at zero.  Calls that overlap on
+ *     the GPU (different streams, or different host threads without ordering)
+ *     race on the buffer: serialise them.
+ * Other arguments and errors as for cpattn_prefill.
+ */
+#define CPATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+cpattn_status cpattn_prefill_noalloc(const cpattn_tensor *q, const cpattn_tensor *k,
+                                     const cpattn_tensor *v, int64_t q_base, int n_chunks,
+                                     int mode, int causal, float scale, cpattn_tensor *o,
+                                     float *lse, void *stream);
+
 /* Human-readable name of a status code (static string). */
 const char *cpattn_status_string(cpattn_status s);
 
