@@ -31,6 +31,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include "cpattn_internal.h"
 #include "epilogue.cuh"
@@ -219,13 +220,18 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&t);
 }
 
 // ---------------------------------------------------------------- kernel
-template <int NT>
+template <int NT, bool kStrictOrder>
 __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnParams p) {
@@ -345,7 +351,16 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
     }
     __syncwarp();
   } else if (warp == L::kMmaWarp) {
-    // ================================================= MMA issuer
+    // ================================================= MMA issuer (one thread)
+    // Issue order per KV step j (ping-pong between the two tiles):
+    //   O_0 += P_0(j) V_j,  S_0(j+1) = Q_0 K_{j+1}^T,  O_1 += P_1(j) V_j,  S_1(j+1) = ...
+    // While tile 0's softmax turns S_0(j+1) into P_0(j+1), the tensor pipe
+    // runs tile 1's two MMAs, and the other way round.
+    // S_t(j+1) overwrites the TMEM columns that hold P_t(j), which the PV MMA
+    // issued just before reads.  The default schedule relies on the tensor
+    // pipe executing one thread's MMAs in issue order (PTX states that order
+    // only for MMAs sharing an accumulator); kStrictOrder inserts a wait for
+    // the PV MMA to complete before S_t(j+1) is issued.
     if (lane == 0 && n_kv > 0) {
       bool ok = wait_bar(bar(L::b_qfull), 0, abort_flag);
       auto issue_qk = [&](int t, int st) {
@@ -380,8 +395,8 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
         const int st = j % kStages;
         const int st1 = (j + 1) % kStages;
         const bool more = j + 1 < n_kv;
-        if (!wait_bar(bar(L::b_vfull + st), (j / kStages) & 1, abort_flag)) { ok = false; break; }
-        if (more && !wait_bar(bar(L::b_kfull + st1), ((j + 1) / kStages) & 1, abort_flag)) {
+        if (!wait_bar(bar(L::b_vfull + st), (j / kStages) & 1, abort_flag) ||
+            (more && !wait_bar(bar(L::b_kfull + st1), ((j + 1) / kStages) & 1, abort_flag))) {
           ok = false;
           break;
         }
@@ -392,9 +407,10 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
           mma_commit(bar(L::b_pvdone + t));
           if (t == NT - 1) mma_commit(bar(L::b_vempty + st));
           if (more) {
-            // S_t(j+1) overwrites the columns that hold P_t(j).
-            if (!wait_bar(bar(L::b_pvdone + t), j & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
+            if (kStrictOrder) {
+              if (!wait_bar(bar(L::b_pvdone + t), j & 1, abort_flag)) { ok = false; break; }
+              tc_fence_after();
+            }
             issue_qk(t, st1);
             mma_commit(bar(L::b_sfull + t));
             if (t == NT - 1) mma_commit(bar(L::b_kempty + st1));
@@ -442,9 +458,18 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
         for (int c = 0; c < kBN; ++c)
           if (c >= nvis) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // Row max: eight independent chains of 3-input maxima (short
+      // dependency chains keep the softmax off the MMA critical path).
+      float mk[8];
 #pragma unroll
-      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+      for (int k = 0; k < 8; ++k) {
+        float m = fmax3(s[k], s[k + 8], s[k + 16]);
+#pragma unroll
+        for (int i = 3; i < 15; i += 2) m = fmax3(m, s[k + 8 * i], s[k + 8 * (i + 1)]);
+        mk[k] = fmaxf(m, s[k + 120]);
+      }
+      const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
+                             fmaxf(mk[6], mk[7]));
       const float m_new = fmaxf(m_run, mx * sl2);
       const bool grow = m_new > m_run + kRescaleLog2;
       float alpha = 1.f;
@@ -465,17 +490,25 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
           tmem_st_x32(t_o + cc * 32, ov);
         }
       }
+      // p = 2^(s * scale * log2e - m): the scale-and-shift runs two columns per
+      // instruction (f32x2 FMA), the row sum in four independent f32x2 chains.
       const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+      const float2 sl2v = make_float2(sl2, sl2);
+      const float2 negm = make_float2(neg_m, neg_m);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
       uint32_t pk[64];
-      float lsum = 0.f;
 #pragma unroll
       for (int c = 0; c < kBN; c += 2) {
-        const float p0 = ex2(fmaf(s[c], sl2, neg_m));
-        const float p1 = ex2(fmaf(s[c + 1], sl2, neg_m));
-        lsum += p0 + p1;
-        pk[c >> 1] = pack_bf16(p0, p1);
+        const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2v, negm);
+        const float2 pv = make_float2(ex2(x.x), ex2(x.y));
+        acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], pv);
+        pk[c >> 1] = pack_bf16(pv.x, pv.y);
       }
-      l_run += lsum;
+      const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+      const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+      const float2 a03 = __fadd2_rn(a01, a23);
+      l_run += a03.x + a03.y;
       tmem_st_x64(t_s, pk);
       tmem_wait_st();
       tc_fence_before();
@@ -554,7 +587,7 @@ bool make_map(CUtensorMap *map, const void *base, int64_t B, int64_t S, int64_t 
   return r == CUDA_SUCCESS;
 }
 
-template <int NT>
+template <int NT, bool kStrictOrder>
 cudaError_t launch_nt(AttnParams &p, cudaStream_t stream) {
   using L = Layout<NT>;
   int total = 0;
@@ -575,13 +608,13 @@ cudaError_t launch_nt(AttnParams &p, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NT>,
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NT, kStrictOrder>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::alloc_bytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  attn_tc_kernel<NT><<<total, L::kThreads, L::alloc_bytes, stream>>>(mq, mk, mv, p);
+  attn_tc_kernel<NT, kStrictOrder><<<total, L::kThreads, L::alloc_bytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -591,10 +624,18 @@ bool attn_tc_supported(const AttnParams &p) {
   return !p.in_f32 && p.D == kD && p.q_rows_total > 0 && p.kv_rows_total > 0;
 }
 
+// CPATTN_STRICT_MMA_ORDER=1 selects the schedule that waits for each PV MMA
+// to complete before the next QK MMA overwrites P (see the MMA issuer).
+bool strict_mma_order() {
+  const char *e = getenv("CPATTN_STRICT_MMA_ORDER");
+  return e != nullptr && e[0] != '\0' && e[0] != '0';
+}
+
 cudaError_t launch_attn_tc(AttnParams &p, cudaStream_t stream) {
   const int g = p.Hq / p.Hkv;
-  if (g % 2 == 0) return launch_nt<2>(p, stream);
-  return launch_nt<1>(p, stream);
+  const bool strict = strict_mma_order();
+  if (g % 2 == 0) return strict ? launch_nt<2, true>(p, stream) : launch_nt<2, false>(p, stream);
+  return strict ? launch_nt<1, true>(p, stream) : launch_nt<1, false>(p, stream);
 }
 
 unsigned int attn_tc_read_status(bool clear, cudaError_t *err) {

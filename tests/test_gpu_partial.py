@@ -150,3 +150,24 @@ def test_argument_errors_do_not_launch(B):
     with pytest.raises(B.CpattnError) as err:
         B.partial(q, q[:, :, :1], q[:, :, :1])
     assert err.value.status == 2   # head_dim 96 unsupported
+
+
+@pytest.mark.parametrize("case", [TC_CASES[1], TC_CASES[2], TC_CASES[4], TC_CASES[5]],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_strict_mma_order_matches_default(B, case, monkeypatch):
+    """The default MMA schedule lets S_t(j+1) follow O_t += P_t(j) V_j without
+    waiting (it relies on the tensor pipe running one thread's MMAs in issue
+    order).  CPATTN_STRICT_MMA_ORDER=1 waits for each PV MMA instead.  Both
+    must give bitwise the same result, and both must match the oracle."""
+    sq, skv, hq, hkv, d, q_off, kv_off, causal = case
+    q = rand((1, sq, hq, d), torch.bfloat16, 21)
+    k = rand((1, skv, hkv, d), torch.bfloat16, 22)
+    v = rand((1, skv, hkv, d), torch.bfloat16, 23)
+    o_fast, l_fast = B.partial(q, k, v, q_off, kv_off, causal, out_dtype=torch.float32)
+    monkeypatch.setenv("CPATTN_STRICT_MMA_ORDER", "1")
+    o_strict, l_strict = B.partial(q, k, v, q_off, kv_off, causal, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(o_fast, o_strict) and torch.equal(l_fast, l_strict)
+    rows = np.arange(sq)
+    ref_o, ref_l = oracle_rows(q, k, v, rows, q_base=q_off, kv_pos0=kv_off, causal=causal)
+    compare(o_strict, l_strict, rows, ref_o, ref_l, TOL["bf16"], f"strict {case}")
