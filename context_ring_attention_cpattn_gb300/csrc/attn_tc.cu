@@ -363,23 +363,29 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
     // the PV MMA to complete before S_t(j+1) is issued.
     if (lane == 0 && n_kv > 0) {
       bool ok = wait_bar(bar(L::b_qfull), 0, abort_flag);
+      // Descriptors of the first 16-column slice of tile 0 / stage 0 of each
+      // operand; other tiles, stages and slices add their byte offset (>> 4)
+      // to the start-address field (shared memory stays below 256 KB, so the
+      // 14-bit field cannot carry).
+      const uint64_t dq0 = make_sdesc(sb + L::q_off, 16, 1024);
+      const uint64_t dk0 = make_sdesc(sb + L::k_off, 16, 1024);
+      const uint64_t dv0 = make_sdesc(sb + L::v_off, kBoxBytes, 1024);
+      constexpr uint64_t kTileStep = kTileBytes >> 4;
       auto issue_qk = [&](int t, int st) {
-        const uint32_t qa = sb + L::q_off + t * kTileBytes;
-        const uint32_t ka = sb + L::k_off + st * kTileBytes;
+        const uint64_t dq = dq0 + (uint64_t)t * kTileStep;
+        const uint64_t dk = dk0 + (uint64_t)st * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + t * 128, make_sdesc(qa + off, 16, 1024), make_sdesc(ka + off, 16, 1024),
-                 kIdescQK, kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+          mma_ss(tmem + t * 128, dq + off, dk + off, kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int st, bool accumulate) {
-        const uint32_t va = sb + L::v_off + st * kTileBytes;
+        const uint64_t dv = dv0 + (uint64_t)st * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           mma_ts(tmem + (NT + t) * 128, tmem + t * 128 + kk * 8,
-                 make_sdesc(va + kk * 16 * 128, kBoxBytes, 1024), kIdescPV,
-                 (accumulate || kk > 0) ? 1u : 0u);
+                 dv + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
         }
       };
       if (ok) ok = wait_bar(bar(L::b_kfull + 0), 0, abort_flag);
@@ -395,22 +401,26 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
         const int st = j % kStages;
         const int st1 = (j + 1) % kStages;
         const bool more = j + 1 < n_kv;
-        if (!wait_bar(bar(L::b_vfull + st), (j / kStages) & 1, abort_flag) ||
-            (more && !wait_bar(bar(L::b_kfull + st1), ((j + 1) / kStages) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
         for (int t = 0; t < NT && ok; ++t) {
-          if (!wait_bar(bar(L::b_pready + t), j & 1, abort_flag)) { ok = false; break; }
+          // Each wait sits right before the first MMA that needs it.
+          if ((t == 0 && !wait_bar(bar(L::b_vfull + st), (j / kStages) & 1, abort_flag)) ||
+              !wait_bar(bar(L::b_pready + t), j & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           issue_pv(t, st, j > 0);
-          mma_commit(bar(L::b_pvdone + t));
           if (t == NT - 1) mma_commit(bar(L::b_vempty + st));
+          if (kStrictOrder || !more) mma_commit(bar(L::b_pvdone + t));
           if (more) {
+            if (t == 0 && !wait_bar(bar(L::b_kfull + st1), ((j + 1) / kStages) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
             if (kStrictOrder) {
               if (!wait_bar(bar(L::b_pvdone + t), j & 1, abort_flag)) { ok = false; break; }
-              tc_fence_after();
             }
+            tc_fence_after();
             issue_qk(t, st1);
             mma_commit(bar(L::b_sfull + t));
             if (t == NT - 1) mma_commit(bar(L::b_kempty + st1));
@@ -518,7 +528,9 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
 
     // ---- epilogue: O_t / l, LSE, routed by the pair's role
     if (ok && n_kv > 0) {
-      ok = __all_sync(0xffffffffu, wait_bar(bar(L::b_pvdone + t), (n_kv - 1) & 1, abort_flag));
+      // pvdone_t completes once per KV step in the strict schedule, else once.
+      const uint32_t par = kStrictOrder ? ((n_kv - 1) & 1) : 0u;
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::b_pvdone + t), par, abort_flag));
       tc_fence_after();
     }
     if (__all_sync(0xffffffffu, ok && !*abort_flag)) {
