@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # DRAM bytes (read + write) per tensor FLOP of the tensor-core attention
 # kernel from one ncu capture, and the kernel source it was taken from; the
 # roofline's traffic is null whenever the source differs from the capture.
-TRAFFIC_RECORD = {"sha": "0930d60a5f646cda", "bytes_per_flop": 3.036e-4,
+TRAFFIC_RECORD = {"sha": "1b7cac6d1c22fe96", "bytes_per_flop": 3.0365e-4,
                   "capture": "profiles/attn_tc_128k_passkv_step2.md"}
 
 
@@ -261,6 +261,37 @@ def time_modes(B, w, q, k, v, outs, wss, steps, warmup, world, modes, profile_ca
     return max_over_ranks(elapsed, world), per_mode, recs
 
 
+def time_merge2(B, w, hbm_peak, peak_src, reps=5):
+    """Pairwise in-place LSE merge (cpattn_merge) of two fp32 partials of the
+    workload's shape; algorithmic bytes = read both sides + write one."""
+    import torch
+
+    shape = (w.batch, w.sq, w.hq, w.head_dim)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    oa = torch.randn(shape, generator=g, device="cuda")
+    ob = torch.randn(shape, generator=g, device="cuda")
+    la = torch.randn((w.batch, w.hq, w.sq), generator=g, device="cuda")
+    lb = torch.randn((w.batch, w.hq, w.sq), generator=g, device="cuda")
+    for _ in range(2):
+        B.merge_(oa, la, ob, lb)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        B.merge_(oa, la, ob, lb)
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = 3.0 * w.batch * w.sq * w.hq * (w.head_dim * 4 + 4)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del oa, ob, la, lb
+    torch.cuda.empty_cache()
+    return {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+            "frac_of_8TBs": gbs / 8000.0, "ms": ms, "bytes_per_launch": nbytes,
+            "shape": "fp32 [%d, %d, %d, %d] both sides" % shape, "peak_source": f"{peak_src} HBM copy"}
+
+
 def make_buffers(B, w, q, k, modes):
     import torch
 
@@ -347,6 +378,17 @@ def main():
                 "share_of_step": tc_ms / elapsed if elapsed else None}
 
     ms_layer = {names[m]: statistics.median(per_mode[m]) for m in modes}
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    mn = [r for r in recs if r[0] == "mergeN"]
+    merge_roofline = {}
+    if mn:
+        gbs = sum(r[2] for r in mn) / (sum(r[1] for r in mn) * 1e-3) / 1e9
+        merge_roofline["mergeN"] = {
+            "bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+            "frac": gbs / hbm_peak, "frac_of_8TBs": gbs / 8000.0, "launches_timed": len(mn),
+            "bytes_per_launch": sum(r[2] for r in mn) / len(mn),
+            "peak_source": f"{peak_src} HBM copy"}
+    merge_roofline["merge2"] = time_merge2(B, w, hbm_peak, peak_src)
     cfg = {"workload": w.name, "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim,
            "seq_len": w.sq, "n_chunks": w.n_chunks, "causal": w.causal,
            "step": " + ".join({"pass_kv": "Pass-KV prefill", "pass_q": "Pass-Q prefill"}[names[m]]
@@ -422,7 +464,8 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic (seeded i.i.d. N(0,1) Q/K/V, bf16)", "config": cfg,
-                "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
+                "roofline": roofline, "merge_roofline": merge_roofline,
+                "cpu_baseline": cpu_baseline, "e2e": e2e,
                 "gpu_launches": len(recs), "clocks": clk}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -64,9 +64,12 @@ __global__ void __launch_bounds__(kWarps * 32) merge2_kernel(const __grid_consta
 
 // Pass-Q: for item x, rows [0, chunk_rows) of Q chunk x merge slots
 // slot0 .. slot0 + count - 1 (ascending KV chunk) into the final output.
+// Each warp keeps kInFlight partial rows' loads outstanding at once, so an
+// SM has enough bytes in flight to approach the copy bandwidth.
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32) mergen_kernel(const __grid_constant__ MergeNParams p) {
   constexpr int E = D / 32;
+  constexpr int kInFlight = 8;
   const int lane = threadIdx.x & 31;
   const int item = blockIdx.y;
   const int count = p.item_count[item];
@@ -77,11 +80,16 @@ __global__ void __launch_bounds__(kWarps * 32) mergen_kernel(const __grid_consta
     const int h = (int)(r % p.H);
     const int64_t s = (r / p.H) % p.chunk_rows;  // chunk-relative row
     const int b = (int)(r / ((int64_t)p.H * p.chunk_rows));
+    const float *lse0 = p.part.lse + (int64_t)slot0 * p.part_lse_stride + (int64_t)b * p.part.lb +
+                        (int64_t)h * p.part.lh + s;
+    const float *o0 = reinterpret_cast<const float *>(p.part.o) + (int64_t)slot0 * p.part_o_stride +
+                      (int64_t)b * p.part.sb + s * p.part.ss + (int64_t)h * p.part.sh + lane * E;
     // Maximum LSE over the parts.
     float m = -INFINITY;
-    for (int j = 0; j < count; ++j) {
-      const float *lse_j = p.part.lse + (int64_t)(slot0 + j) * p.part_lse_stride;
-      m = fmaxf(m, lse_j[(int64_t)b * p.part.lb + (int64_t)h * p.part.lh + s]);
+    for (int j0 = 0; j0 < count; j0 += kInFlight) {
+#pragma unroll
+      for (int u = 0; u < kInFlight; ++u)
+        if (j0 + u < count) m = fmaxf(m, lse0[(int64_t)(j0 + u) * p.part_lse_stride]);
     }
     float acc[E];
 #pragma unroll
@@ -89,17 +97,27 @@ __global__ void __launch_bounds__(kWarps * 32) mergen_kernel(const __grid_consta
     float lse_out = -INFINITY;
     if (m != -INFINITY) {
       float sum = 0.f;
-      for (int j = 0; j < count; ++j) {
-        const float *lse_j = p.part.lse + (int64_t)(slot0 + j) * p.part_lse_stride;
-        const float e = expf(lse_j[(int64_t)b * p.part.lb + (int64_t)h * p.part.lh + s] - m);
-        sum += e;
-        const float *o_j = reinterpret_cast<const float *>(p.part.o) +
-                           (int64_t)(slot0 + j) * p.part_o_stride + (int64_t)b * p.part.sb +
-                           s * p.part.ss + (int64_t)h * p.part.sh;
-        float v[E];
-        load_f32<E>(o_j, lane * E, v);
+      for (int j0 = 0; j0 < count; j0 += kInFlight) {
+        float l[kInFlight];
+        float v[kInFlight][E];
 #pragma unroll
-        for (int i = 0; i < E; ++i) acc[i] = fmaf(e, v[i], acc[i]);
+        for (int u = 0; u < kInFlight; ++u) {
+          if (j0 + u < count) {
+            l[u] = lse0[(int64_t)(j0 + u) * p.part_lse_stride];
+            load_f32<E>(o0 + (int64_t)(j0 + u) * p.part_o_stride, 0, v[u]);
+          } else {
+            l[u] = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < E; ++i) v[u][i] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kInFlight; ++u) {
+          const float e = expf(l[u] - m);  // 0 for padding and empty parts
+          sum += e;
+#pragma unroll
+          for (int i = 0; i < E; ++i) acc[i] = fmaf(e, v[u][i], acc[i]);
+        }
       }
       const float inv = 1.f / sum;
 #pragma unroll
