@@ -352,7 +352,12 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
   double bytes = 0.0;
   const double row_bytes = (double)q->b * pl.Cq * q->h * (q->d * 4.0 + 4.0);
   const double out_bytes = (double)q->b * pl.Cq * q->h * (q->d * elem_bytes(o->dtype) + 4.0);
-  for (int i = 0; i < pl.N; ++i) {
+  // Items with the most partials first (longest CTAs first).
+  std::vector<int> order(pl.N);
+  for (int i = 0; i < pl.N; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int b) { return pl.count[a] > pl.count[b]; });
+  for (int i : order) {
     const bool merge = pl.mode == CPATTN_PASS_Q && pl.count[i] >= 2;
     if (!merge && pl.count[i] != 0) continue;
     mp.item_row0[mp.n_items] = (int32_t)(i * pl.Cq);

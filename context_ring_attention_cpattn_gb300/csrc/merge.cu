@@ -12,7 +12,9 @@
 // Mapping: one warp per (batch, row, head) vector of D values, lanes own D/32
 // consecutive columns (16-byte fp32 loads at D = 128), consecutive warps walk
 // consecutive rows of the [b, s, h, d] layout, so every request is a fully
-// used, coalesced 512-byte line.  fp32 arithmetic, output rounded once.
+// used, coalesced 512-byte line.  Grids cover all rows with short CTAs (no
+// grid-stride loop), so uneven per-row work is balanced by the scheduler.
+// fp32 arithmetic, output rounded once.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -23,6 +25,7 @@ namespace cpattn {
 namespace {
 
 constexpr int kWarps = 8;
+constexpr int kRowsPerWarp = 2;  // rows per warp, loads of all of them in flight together
 
 template <int E>
 __device__ __forceinline__ void load_row(const OutView &w, int b, int64_t row, int h, int c0,
@@ -37,35 +40,47 @@ __device__ __forceinline__ void load_row(const OutView &w, int b, int64_t row, i
   }
 }
 
-// (a) <- merge(a, b), element-wise over rows.
+// (a) <- merge(a, b), element-wise over rows.  Each warp merges kRowsPerWarp
+// rows with all their loads issued before any arithmetic.
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32) merge2_kernel(const __grid_constant__ Merge2Params p) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
   const int64_t n_rows = (int64_t)p.B * p.S * p.H;
-  for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < n_rows;
-       r += (int64_t)gridDim.x * kWarps) {
-    const int h = (int)(r % p.H);
-    const int64_t s = (r / p.H) % p.S;
-    const int b = (int)(r / ((int64_t)p.H * p.S));
-    float *la = view_lse(p.a, b, s, h);
-    const float lb = *view_lse(p.b, b, s, h);
-    const MergeW w = merge_weights(*la, lb);
-    float va[E], vb[E];
-    load_row<E>(p.a, b, s, h, lane * E, va);
-    load_row<E>(p.b, b, s, h, lane * E, vb);
+  const int64_t r0 = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRowsPerWarp;
+  float va[kRowsPerWarp][E], vb[kRowsPerWarp][E], la[kRowsPerWarp], lb[kRowsPerWarp];
+  int hh[kRowsPerWarp], bb[kRowsPerWarp];
+  int64_t ss[kRowsPerWarp];
 #pragma unroll
-    for (int i = 0; i < E; ++i) va[i] = __fmul_rn(w.wa, va[i]) + __fmul_rn(w.wb, vb[i]);
+  for (int u = 0; u < kRowsPerWarp; ++u) {
+    const int64_t r = r0 + u;
+    if (r >= n_rows) break;
+    hh[u] = (int)(r % p.H);
+    ss[u] = (r / p.H) % p.S;
+    bb[u] = (int)(r / ((int64_t)p.H * p.S));
+    la[u] = *view_lse(p.a, bb[u], ss[u], hh[u]);
+    lb[u] = *view_lse(p.b, bb[u], ss[u], hh[u]);
+    load_row<E>(p.a, bb[u], ss[u], hh[u], lane * E, va[u]);
+    load_row<E>(p.b, bb[u], ss[u], hh[u], lane * E, vb[u]);
+  }
+#pragma unroll
+  for (int u = 0; u < kRowsPerWarp; ++u) {
+    if (r0 + u >= n_rows) break;
+    const MergeW w = merge_weights(la[u], lb[u]);
+#pragma unroll
+    for (int i = 0; i < E; ++i) va[u][i] = __fmul_rn(w.wa, va[u][i]) + __fmul_rn(w.wb, vb[u][i]);
     __syncwarp();
-    store_vals<E>(view_row(p.a, b, s, h), p.a.f32, lane * E, va);
-    if (lane == 0) *la = w.lse;
+    store_vals<E>(view_row(p.a, bb[u], ss[u], hh[u]), p.a.f32, lane * E, va[u]);
+    if (lane == 0) *view_lse(p.a, bb[u], ss[u], hh[u]) = w.lse;
   }
 }
 
 // Pass-Q: for item x, rows [0, chunk_rows) of Q chunk x merge slots
 // slot0 .. slot0 + count - 1 (ascending KV chunk) into the final output.
-// Each warp keeps kInFlight partial rows' loads outstanding at once, so an
-// SM has enough bytes in flight to approach the copy bandwidth.
+// One pass with a running maximum: every group of kInFlight partials (their
+// LSE and O rows, for kRowsPerWarp rows at once) is loaded before any of it
+// is used, so each warp keeps up to kRowsPerWarp * kInFlight 512-byte rows in
+// flight and pays one memory round trip per group.
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32) mergen_kernel(const __grid_constant__ MergeNParams p) {
   constexpr int E = D / 32;
@@ -75,68 +90,81 @@ __global__ void __launch_bounds__(kWarps * 32) mergen_kernel(const __grid_consta
   const int count = p.item_count[item];
   const int slot0 = p.item_slot0[item];
   const int64_t n_rows = (int64_t)p.B * p.chunk_rows * p.H;
-  for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < n_rows;
-       r += (int64_t)gridDim.x * kWarps) {
+  const int64_t r0 = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRowsPerWarp;
+  if (r0 >= n_rows) return;
+  const float *lse0[kRowsPerWarp];
+  const float *o0[kRowsPerWarp];
+  float m[kRowsPerWarp], sum[kRowsPerWarp], acc[kRowsPerWarp][E];
+#pragma unroll
+  for (int u = 0; u < kRowsPerWarp; ++u) {
+    const int64_t r = r0 + u < n_rows ? r0 + u : r0;  // a duplicate row is computed, not stored
     const int h = (int)(r % p.H);
-    const int64_t s = (r / p.H) % p.chunk_rows;  // chunk-relative row
+    const int64_t s = (r / p.H) % p.chunk_rows;
     const int b = (int)(r / ((int64_t)p.H * p.chunk_rows));
-    const float *lse0 = p.part.lse + (int64_t)slot0 * p.part_lse_stride + (int64_t)b * p.part.lb +
-                        (int64_t)h * p.part.lh + s;
-    const float *o0 = reinterpret_cast<const float *>(p.part.o) + (int64_t)slot0 * p.part_o_stride +
-                      (int64_t)b * p.part.sb + s * p.part.ss + (int64_t)h * p.part.sh + lane * E;
-    // Maximum LSE over the parts.
-    float m = -INFINITY;
-    for (int j0 = 0; j0 < count; j0 += kInFlight) {
+    lse0[u] = p.part.lse + (int64_t)slot0 * p.part_lse_stride + (int64_t)b * p.part.lb +
+              (int64_t)h * p.part.lh + s;
+    o0[u] = reinterpret_cast<const float *>(p.part.o) + (int64_t)slot0 * p.part_o_stride +
+            (int64_t)b * p.part.sb + s * p.part.ss + (int64_t)h * p.part.sh + lane * E;
+    m[u] = -INFINITY;
+    sum[u] = 0.f;
 #pragma unroll
-      for (int u = 0; u < kInFlight; ++u)
-        if (j0 + u < count) m = fmaxf(m, lse0[(int64_t)(j0 + u) * p.part_lse_stride]);
-    }
-    float acc[E];
+    for (int i = 0; i < E; ++i) acc[u][i] = 0.f;
+  }
+  for (int j0 = 0; j0 < count; j0 += kInFlight) {
+    float l[kRowsPerWarp][kInFlight];
+    float v[kRowsPerWarp][kInFlight][E];
 #pragma unroll
-    for (int i = 0; i < E; ++i) acc[i] = 0.f;
-    float lse_out = -INFINITY;
-    if (m != -INFINITY) {
-      float sum = 0.f;
-      for (int j0 = 0; j0 < count; j0 += kInFlight) {
-        float l[kInFlight];
-        float v[kInFlight][E];
+    for (int u = 0; u < kRowsPerWarp; ++u)
 #pragma unroll
-        for (int u = 0; u < kInFlight; ++u) {
-          if (j0 + u < count) {
-            l[u] = lse0[(int64_t)(j0 + u) * p.part_lse_stride];
-            load_f32<E>(o0 + (int64_t)(j0 + u) * p.part_o_stride, 0, v[u]);
-          } else {
-            l[u] = -INFINITY;
+      for (int x = 0; x < kInFlight; ++x) {
+        if (j0 + x < count) {
+          l[u][x] = lse0[u][(int64_t)(j0 + x) * p.part_lse_stride];
+          load_f32<E>(o0[u] + (int64_t)(j0 + x) * p.part_o_stride, 0, v[u][x]);
+        } else {
+          l[u][x] = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < E; ++i) v[u][i] = 0.f;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kInFlight; ++u) {
-          const float e = expf(l[u] - m);  // 0 for padding and empty parts
-          sum += e;
-#pragma unroll
-          for (int i = 0; i < E; ++i) acc[i] = fmaf(e, v[u][i], acc[i]);
+          for (int i = 0; i < E; ++i) v[u][x][i] = 0.f;
         }
       }
-      const float inv = 1.f / sum;
 #pragma unroll
-      for (int i = 0; i < E; ++i) acc[i] *= inv;
-      lse_out = m + logf(sum);
+    for (int u = 0; u < kRowsPerWarp; ++u) {
+      float mg = l[u][0];
+#pragma unroll
+      for (int x = 1; x < kInFlight; ++x) mg = fmaxf(mg, l[u][x]);
+      const float m_new = fmaxf(m[u], mg);
+      if (m_new == -INFINITY) continue;  // nothing visible yet
+      const float c = expf(m[u] - m_new);  // 0 when m = -inf
+      sum[u] *= c;
+#pragma unroll
+      for (int i = 0; i < E; ++i) acc[u][i] *= c;
+#pragma unroll
+      for (int x = 0; x < kInFlight; ++x) {
+        const float e = expf(l[u][x] - m_new);  // 0 for padding and empty parts
+        sum[u] += e;
+#pragma unroll
+        for (int i = 0; i < E; ++i) acc[u][i] = fmaf(e, v[u][x][i], acc[u][i]);
+      }
+      m[u] = m_new;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kRowsPerWarp; ++u) {
+    const int64_t r = r0 + u;
+    if (r >= n_rows) break;
+    const int h = (int)(r % p.H);
+    const int64_t s = (r / p.H) % p.chunk_rows;
+    const int b = (int)(r / ((int64_t)p.H * p.chunk_rows));
+    float lse_out = -INFINITY;
+    if (m[u] != -INFINITY) {
+      const float inv = 1.f / sum[u];
+#pragma unroll
+      for (int i = 0; i < E; ++i) acc[u][i] *= inv;
+      lse_out = m[u] + logf(sum[u]);
     }
     const int64_t abs_row = (int64_t)p.item_row0[item] + s;
-    store_vals<E>(view_row(p.out, b, abs_row, h), p.out.f32, lane * E, acc);
+    store_vals<E>(view_row(p.out, b, abs_row, h), p.out.f32, lane * E, acc[u]);
     if (lane == 0) *view_lse(p.out, b, abs_row, h) = lse_out;
   }
-}
-
-int grid_for(int64_t n_rows) {
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t want = (n_rows + kWarps - 1) / kWarps;
-  const int64_t cap = (int64_t)sms * 8;  // 8 resident CTAs of 256 threads per SM
-  return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
 }  // namespace
@@ -144,11 +172,12 @@ int grid_for(int64_t n_rows) {
 cudaError_t launch_merge_2(const Merge2Params &p, cudaStream_t stream) {
   const int64_t n_rows = (int64_t)p.B * p.S * p.H;
   if (n_rows == 0) return cudaSuccess;
-  const int grid = grid_for(n_rows);
+  const int64_t per_cta = (int64_t)kWarps * kRowsPerWarp;
+  const int64_t grid = (n_rows + per_cta - 1) / per_cta;
   if (p.D == 128) {
-    merge2_kernel<128><<<grid, kWarps * 32, 0, stream>>>(p);
+    merge2_kernel<128><<<(unsigned)grid, kWarps * 32, 0, stream>>>(p);
   } else if (p.D == 64) {
-    merge2_kernel<64><<<grid, kWarps * 32, 0, stream>>>(p);
+    merge2_kernel<64><<<(unsigned)grid, kWarps * 32, 0, stream>>>(p);
   } else {
     return cudaErrorInvalidValue;
   }
@@ -158,9 +187,8 @@ cudaError_t launch_merge_2(const Merge2Params &p, cudaStream_t stream) {
 cudaError_t launch_merge_n(const MergeNParams &p, cudaStream_t stream) {
   const int64_t n_rows = (int64_t)p.B * p.chunk_rows * p.H;
   if (n_rows == 0 || p.n_items == 0) return cudaSuccess;
-  int gx = grid_for(n_rows * p.n_items);
-  gx = (gx + p.n_items - 1) / p.n_items;
-  dim3 grid(gx, p.n_items);
+  const int64_t per_cta = (int64_t)kWarps * kRowsPerWarp;
+  dim3 grid((unsigned)((n_rows + per_cta - 1) / per_cta), p.n_items);
   if (p.D == 128) {
     mergen_kernel<128><<<grid, kWarps * 32, 0, stream>>>(p);
   } else if (p.D == 64) {
