@@ -292,6 +292,62 @@ def time_merge2(B, w, hbm_peak, peak_src, reps=5):
             "shape": "fp32 [%d, %d, %d, %d] both sides" % shape, "peak_source": f"{peak_src} HBM copy"}
 
 
+def time_decode(B, steps, hbm_peak, peak_src, name="decode-128k-b8"):
+    """Pass-Q decode (cpattn_decode) of one token per sequence against a
+    CP-sharded cache: HBM-bound; algorithmic bytes = visible K and V + Q + O,
+    plus the fp32 partials written and re-read by the merge."""
+    import torch
+
+    from context_ring_attention_cpattn_gb300.workloads import WORKLOADS, make_qkv
+
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty((w.batch, w.hq, w.sq), dtype=torch.float32, device="cuda")
+    need = B.decode_workspace_size(q, k, w.n_chunks, w.q_base, w.causal)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+
+    def run():
+        B.decode(q, k, v, w.n_chunks, q_base=w.q_base, causal=w.causal, out=out, lse=lse,
+                 workspace=ws)
+
+    for _ in range(5):
+        run()
+    torch.cuda.synchronize()
+    n = max(20, steps * 4)
+    # Flush L2 between calls so each one streams the cache from HBM (K/V are
+    # 512 MiB in total, larger than L2, but the tail of one call is still
+    # resident at the start of the next).
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    B.profile_begin(4 * n)
+    evs = []
+    for _ in range(n):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run()
+        e1.record()
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    recs = B.profile_end(4 * n)
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    vis = min(w.q_base + w.sq, w.skv)
+    kv_bytes = 2.0 * w.batch * vis * w.hkv * w.head_dim * 2
+    part_bytes = need  # fp32 partials: written once, read once
+    qo_bytes = 2.0 * w.batch * w.sq * w.hq * w.head_dim * 2
+    total = kv_bytes + 2.0 * part_bytes + qo_bytes
+    attn = [r for r in recs if r[0] == "attn_tc"]
+    attn_ms = statistics.median(r[1] for r in attn) if attn else None
+    del q, k, v, out, ws, flush
+    torch.cuda.empty_cache()
+    return {"workload": name, "ms_per_call": ms, "tokens_per_s": w.batch * w.sq / (ms * 1e-3),
+            "achieved": total / (ms * 1e-3) / 1e9, "unit": "GB/s", "peak": hbm_peak,
+            "frac": total / (ms * 1e-3) / 1e9 / hbm_peak, "bytes_per_call": total,
+            "attn_kernel": {"ms": attn_ms, "kv_GBs": (kv_bytes / (attn_ms * 1e-3) / 1e9) if attn_ms else None,
+                            "frac": (kv_bytes / (attn_ms * 1e-3) / 1e9 / hbm_peak) if attn_ms else None},
+            "l2": "256 MiB written between calls (L2 flush)", "peak_source": f"{peak_src} HBM copy"}
+
+
 def make_buffers(B, w, q, k, modes):
     import torch
 
@@ -313,6 +369,7 @@ def main():
     ap.add_argument("--workload", default="128k")
     ap.add_argument("--skip-1m", action="store_true", help="do not time the 1M-token layer")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-decode", action="store_true", help="do not time the decode leg")
     ap.add_argument("--schedules", default="both", choices=["both", "kv", "q"],
                     help="ring schedules in one step (default: Pass-KV then Pass-Q)")
     ap.add_argument("--cpu-rows", type=int, default=2048,
@@ -389,6 +446,7 @@ def main():
             "bytes_per_launch": sum(r[2] for r in mn) / len(mn),
             "peak_source": f"{peak_src} HBM copy"}
     merge_roofline["merge2"] = time_merge2(B, w, hbm_peak, peak_src)
+    decode = None if args.skip_decode else time_decode(B, args.steps, hbm_peak, peak_src)
     cfg = {"workload": w.name, "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim,
            "seq_len": w.sq, "n_chunks": w.n_chunks, "causal": w.causal,
            "step": " + ".join({"pass_kv": "Pass-KV prefill", "pass_q": "Pass-Q prefill"}[names[m]]
@@ -464,7 +522,7 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic (seeded i.i.d. N(0,1) Q/K/V, bf16)", "config": cfg,
-                "roofline": roofline, "merge_roofline": merge_roofline,
+                "roofline": roofline, "merge_roofline": merge_roofline, "decode": decode,
                 "cpu_baseline": cpu_baseline, "e2e": e2e,
                 "gpu_launches": len(recs), "clocks": clk}
         print(json.dumps(line), flush=True)

@@ -37,7 +37,8 @@ class ProfileRecord(ctypes.Structure):
 
 EXPORTED = ["cpattn_partial", "cpattn_merge", "cpattn_prefill_workspace_size", "cpattn_prefill",
             "cpattn_prefill_plan", "cpattn_prefill_host_scratch_size", "cpattn_prefill_host",
-            "cpattn_prefill_noalloc", "cpattn_status_string", "cpattn_device_status",
+            "cpattn_prefill_noalloc", "cpattn_decode_workspace_size", "cpattn_decode",
+            "cpattn_status_string", "cpattn_device_status",
             "cpattn_profile_begin", "cpattn_profile_end"]
 
 _lib = None
@@ -76,6 +77,8 @@ def lib():
     L.cpattn_prefill_host.argtypes = [T, T, T, i64, i32, i32, i32, f32, T, vp, vp, ctypes.c_size_t,
                                       vp]
     L.cpattn_prefill_noalloc.argtypes = [T, T, T, i64, i32, i32, i32, f32, T, vp, vp]
+    L.cpattn_decode_workspace_size.argtypes = [T, T, i64, i32, i32, sz]
+    L.cpattn_decode.argtypes = [T, T, T, i64, i32, i32, f32, T, vp, vp, ctypes.c_size_t, vp]
     L.cpattn_status_string.argtypes = [i32]
     L.cpattn_status_string.restype = ctypes.c_char_p
     L.cpattn_device_status.argtypes = [i32]
@@ -176,6 +179,38 @@ def prefill(q, k, v, n_chunks: int, mode: int, q_base: int = 0, causal: bool = T
                                 int(q_base), int(n_chunks), int(mode), int(bool(causal)),
                                 float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(), ws_ptr,
                                 ws_len, _stream(stream)), "cpattn_prefill")
+    return out, lse
+
+
+def decode_workspace_size(q, k, n_chunks: int, q_base: int = 0, causal: bool = True) -> int:
+    n = ctypes.c_size_t(0)
+    qv, kv_ = view(q), view(k)
+    _check(lib().cpattn_decode_workspace_size(ctypes.byref(qv), ctypes.byref(kv_), int(q_base),
+                                              int(n_chunks), int(bool(causal)), ctypes.byref(n)),
+           "cpattn_decode_workspace_size")
+    return n.value
+
+
+def decode(q, k, v, n_chunks: int, q_base: int = 0, causal: bool = True, scale=None, out=None,
+           lse=None, workspace=None, out_dtype=None, stream=None):
+    """Pass-Q decode of a few query tokens against a CP-sharded KV cache; see cpattn_decode."""
+    import torch
+
+    B, S, H, D = q.shape
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=out_dtype or q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    need = decode_workspace_size(q, k, n_chunks, q_base, causal)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    qv, kv_, vv, ov = view(q), view(k), view(v), view(out)
+    _check(lib().cpattn_decode(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv), int(q_base),
+                               int(n_chunks), int(bool(causal)), float(scale or 0.0),
+                               ctypes.byref(ov), lse.data_ptr(), ws_ptr, ws_len, _stream(stream)),
+           "cpattn_decode")
     return out, lse
 
 

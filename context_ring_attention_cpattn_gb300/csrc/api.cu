@@ -375,6 +375,67 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
   return CPATTN_OK;
 }
 
+// ----------------------------------------------------------------- decode
+// Pass-Q decode: n_tok query tokens (the same Q on every emulated CP rank)
+// against n_chunks KV chunks.  Every rank splits the part of its chunk that a
+// token can see into kv_split-key pieces; each piece yields an fp32 partial,
+// and all partials are merged by LSE in ascending (chunk, piece) order.
+struct DecodePlan {
+  int64_t C = 0;
+  int kv_split = 0;
+  bool packed = false;              // tensor-core kernel with GQA-packed rows
+  std::vector<int> chunk, vis, slot0;  // visible chunks, visible keys, first slot
+  int n_slots = 0;
+};
+
+constexpr int64_t kDecodeTargetCtas = 1024;  // pieces x kv heads x batch per launch
+
+bool decode_packed_ok(const cpattn_tensor *q, const cpattn_tensor *k) {
+  if (q->dtype != CPATTN_BF16 || q->d != 128 || k->s == 0) return false;
+  const int64_t g = q->h / k->h;
+  return 128 % g == 0 && q->s <= 128 / g;
+}
+
+cpattn_status build_decode_plan(const cpattn_tensor *q, const cpattn_tensor *k, int64_t q_base,
+                                int n_chunks, int causal, DecodePlan &dp) {
+  if (n_chunks < 1 || n_chunks > kMaxPairs) return CPATTN_ERR_INVALID_ARG;
+  if (k->s % n_chunks != 0) return CPATTN_ERR_INVALID_ARG;
+  if (q_base < -kMaxRows * 4 || q_base > kMaxRows * 4) return CPATTN_ERR_UNSUPPORTED;
+  dp.C = k->s / n_chunks;
+  dp.packed = decode_packed_ok(q, k);
+  int64_t total = 0;
+  for (int j = 0; j < n_chunks && q->s > 0 && dp.C > 0; ++j) {
+    int64_t vis = dp.C;
+    if (causal) {
+      const int64_t last = q_base + q->s - 1 - (int64_t)j * dp.C + 1;  // keys the last token sees
+      vis = last < 0 ? 0 : (last < dp.C ? last : dp.C);
+    }
+    if (vis == 0) continue;
+    dp.chunk.push_back(j);
+    dp.vis.push_back((int)vis);
+    total += vis;
+  }
+  if (dp.packed) {
+    int64_t want = (total * k->h * q->b + kDecodeTargetCtas - 1) / kDecodeTargetCtas;
+    want = (want + 127) / 128 * 128;
+    dp.kv_split = (int)std::min<int64_t>(std::max<int64_t>(want, 256), 65536);
+  } else {
+    dp.kv_split = (int)std::max<int64_t>(dp.C, 1);  // one piece per chunk
+  }
+  dp.n_slots = 0;
+  for (size_t x = 0; x < dp.chunk.size(); ++x) {
+    dp.slot0.push_back(dp.n_slots);
+    dp.n_slots += (dp.vis[x] + dp.kv_split - 1) / dp.kv_split;
+  }
+  return CPATTN_OK;
+}
+
+size_t decode_ws_bytes(const DecodePlan &dp, const cpattn_tensor *q) {
+  const size_t o = (size_t)dp.n_slots * q->b * q->s * q->h * q->d * 4;
+  const size_t l = (size_t)dp.n_slots * q->b * q->h * q->s * 4;
+  return align256(o) + align256(l);
+}
+
 size_t tensor_bytes(const cpattn_tensor *t) {
   return (size_t)t->b * t->s * t->h * t->d * elem_bytes(t->dtype);
 }
@@ -493,6 +554,99 @@ cpattn_status cpattn_prefill(const cpattn_tensor *q, const cpattn_tensor *k,
   try {
     return prefill_impl(q, k, v, q_base, n_chunks, mode, causal, scale, o, lse, workspace,
                         workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+  } catch (...) {
+    return CPATTN_ERR_INVALID_ARG;
+  }
+}
+
+cpattn_status cpattn_decode_workspace_size(const cpattn_tensor *q, const cpattn_tensor *k,
+                                           int64_t q_base, int n_chunks, int causal,
+                                           size_t *bytes) {
+  try {
+    if (bytes == nullptr) return CPATTN_ERR_INVALID_ARG;
+    cpattn_status s = check_view(q);
+    if (s != CPATTN_OK) return s;
+    if ((s = check_view(k)) != CPATTN_OK) return s;
+    if (q->h % k->h != 0) return CPATTN_ERR_INVALID_ARG;
+    DecodePlan dp;
+    if ((s = build_decode_plan(q, k, q_base, n_chunks, causal, dp)) != CPATTN_OK) return s;
+    *bytes = decode_ws_bytes(dp, q);
+    return CPATTN_OK;
+  } catch (...) {
+    return CPATTN_ERR_INVALID_ARG;
+  }
+}
+
+cpattn_status cpattn_decode(const cpattn_tensor *q, const cpattn_tensor *k, const cpattn_tensor *v,
+                            int64_t q_base, int n_chunks, int causal, float scale,
+                            cpattn_tensor *o, float *lse, void *workspace, size_t workspace_bytes,
+                            void *stream) {
+  try {
+    cpattn_status s = check_qkv(q, k, v);
+    if (s != CPATTN_OK) return s;
+    if ((s = check_out(o, lse, q)) != CPATTN_OK) return s;
+    DecodePlan dp;
+    if ((s = build_decode_plan(q, k, q_base, n_chunks, causal, dp)) != CPATTN_OK) return s;
+    const size_t need = decode_ws_bytes(dp, q);
+    if (dp.n_slots > 0) {
+      if (workspace == nullptr || workspace_bytes < need) return CPATTN_ERR_WORKSPACE;
+      if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return CPATTN_ERR_WORKSPACE;
+    }
+    if (q->s == 0) return CPATTN_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+    AttnParams p;
+    fill_inputs(p, q, k, v, causal, scale);
+    p.out = out_view(o, lse);
+    if (dp.n_slots > 0) {
+      const size_t o_bytes = (size_t)dp.n_slots * q->b * q->s * q->h * q->d * 4;
+      p.part.o = ws;
+      p.part.lse = reinterpret_cast<float *>(ws + align256(o_bytes));
+      p.part.sh = q->d;
+      p.part.ss = q->h * q->d;
+      p.part.sb = q->s * q->h * q->d;
+      p.part.lh = q->s;
+      p.part.lb = q->h * q->s;
+      p.part.f32 = 1;
+      p.part_o_stride = q->b * q->s * q->h * q->d;
+      p.part_lse_stride = q->b * q->h * q->s;
+      p.n_pairs = (int32_t)dp.chunk.size();
+      for (size_t x = 0; x < dp.chunk.size(); ++x) {
+        PairDesc &pd = p.pairs[x];
+        pd.q_row0 = 0;
+        pd.q_len = (int32_t)q->s;
+        pd.kv_row0 = (int32_t)(dp.chunk[x] * dp.C);
+        pd.kv_len = dp.vis[x];
+        pd.delta = q_base - (int64_t)dp.chunk[x] * dp.C;
+        pd.mode = kPartial;
+        pd.slot = dp.slot0[x];
+      }
+      if (dp.packed) {
+        p.pack_g = (int32_t)(q->h / k->h);
+        p.kv_split = dp.kv_split;
+      }
+      if (launch_attn(p, st, q) != cudaSuccess) return CPATTN_ERR_CUDA;
+    }
+    MergeNParams mp;
+    memset(&mp, 0, sizeof(mp));
+    mp.B = (int32_t)q->b;
+    mp.H = (int32_t)q->h;
+    mp.D = (int32_t)q->d;
+    mp.chunk_rows = (int32_t)q->s;
+    mp.out = p.out;
+    mp.part = p.part;
+    mp.part_o_stride = p.part_o_stride;
+    mp.part_lse_stride = p.part_lse_stride;
+    mp.n_items = 1;
+    mp.item_row0[0] = 0;
+    mp.item_slot0[0] = 0;
+    mp.item_count[0] = dp.n_slots;
+    const double bytes = (double)dp.n_slots * q->b * q->s * q->h * (q->d * 4.0 + 4.0) +
+                         (double)q->b * q->s * q->h * (q->d * elem_bytes(o->dtype) + 4.0);
+    prof_before(st);
+    cudaError_t e = launch_merge_n(mp, st);
+    prof_after(st, CPATTN_KERNEL_MERGEN, bytes);
+    return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
   } catch (...) {
     return CPATTN_ERR_INVALID_ARG;
   }

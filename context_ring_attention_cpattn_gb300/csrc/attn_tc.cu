@@ -46,7 +46,6 @@ namespace {
 constexpr int kBM = 128;                  // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;                  // keys per tile
 constexpr int kD = 128;                   // head dim
-constexpr int kStages = 2;                // K and V ring depth
 constexpr int kBoxBytes = 128 * 128;      // 128 rows x 64 bf16 (one swizzle span)
 constexpr int kTileBytes = 2 * kBoxBytes; // 128 x 128 bf16
 constexpr float kRescaleLog2 = 8.0f;      // lazy-rescale threshold (log2 units)
@@ -54,6 +53,9 @@ constexpr unsigned long long kWaitNs = 2000000000ull;
 
 template <int NT>
 struct Layout {
+  // K and V ring depth: two stages with two query tiles (Q takes 64 KB), three
+  // with one (decode tiles stream K/V and want more copies in flight).
+  static constexpr int kStages = NT == 2 ? 2 : 3;
   static constexpr int kThreads = (4 * NT + 2) * 32;
   static constexpr int kTmaWarp = 4 * NT;
   static constexpr int kMmaWarp = 4 * NT + 1;
@@ -245,39 +247,55 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work item: (pair, query tile, head group, batch)
+  // ---- work item
+  //   per-head tiles (pack_g == 0): (pair, query tile, head group, batch)
+  //   packed decode tiles (pack_g > 0, NT == 1): (pair, kv split, kv head, batch)
   int pi = 0;
   while (pi + 1 < p.n_pairs && (int)blockIdx.x >= p.pairs[pi + 1].cta_begin) ++pi;
   const PairDesc &pd = p.pairs[pi];
   int local = (int)blockIdx.x - pd.cta_begin;
-  const int n_hg = p.Hq / NT;
-  const int hg = local % n_hg;
-  local /= n_hg;
+  const int G = NT == 1 ? p.pack_g : 0;  // query heads per tile in packed mode, else 0
+  int h0, hk, i0, q_rows, split = 0;
+  int64_t ks = 0, ke = pd.kv_len;  // this CTA's keys [ks, ke) of the pair
+  if (G == 0) {
+    const int n_hg = p.Hq / NT;
+    const int hg = local % n_hg;
+    local /= n_hg;
+    const int qt = pd.n_qtiles - 1 - local / p.B;  // longest tiles first
+    h0 = hg * NT;
+    hk = h0 / (p.Hq / p.Hkv);
+    i0 = qt * kBM;
+    q_rows = min(kBM, pd.q_len - i0);
+  } else {
+    hk = local % p.Hkv;
+    local /= p.Hkv;
+    split = local / p.B;
+    h0 = hk * G;
+    i0 = 0;
+    q_rows = pd.q_len;
+    ks = (int64_t)split * p.kv_split;
+    ke = ks + p.kv_split < ke ? ks + p.kv_split : ke;
+  }
   const int b = local % p.B;
-  const int qt = pd.n_qtiles - 1 - local / p.B;  // longest tiles first
-  const int h0 = hg * NT;
-  const int hk = h0 / (p.Hq / p.Hkv);
-  const int i0 = qt * kBM;
-  const int q_rows = min(kBM, pd.q_len - i0);
 
-  // Keys [0, kv_end) are visible to some row of the tile; keys [0, full_end)
+  // Keys [ks, kv_end) are visible to some row of the tile; keys [ks, full_end)
   // to every row.
-  int64_t kv_end = pd.kv_len, full_end = pd.kv_len;
+  int64_t kv_end = ke, full_end = ke;
   if (p.causal) {
     const int64_t last_lim = (int64_t)(i0 + q_rows - 1) + pd.delta + 1;
     const int64_t first_lim = (int64_t)i0 + pd.delta + 1;
     kv_end = last_lim < kv_end ? last_lim : kv_end;
     full_end = first_lim < full_end ? first_lim : full_end;
   }
-  if (kv_end < 0) kv_end = 0;
-  if (full_end < 0) full_end = 0;
-  const int n_kv = (int)((kv_end + kBN - 1) / kBN);
-  const int n_unmasked = (int)(full_end / kBN);
+  if (kv_end < ks) kv_end = ks;
+  if (full_end < ks) full_end = ks;
+  const int n_kv = (int)((kv_end - ks + kBN - 1) / kBN);
+  const int n_unmasked = (int)((full_end - ks) / kBN);
 
   // ---- setup
   if (threadIdx.x == 0) {
     mbar_init(bar(L::b_qfull), 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::b_kfull + s), 1);
       mbar_init(bar(L::b_kempty + s), 1);
       mbar_init(bar(L::b_vfull + s), 1);
@@ -310,18 +328,18 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
   if (warp == L::kTmaWarp) {
     // ================================================= TMA producer
     if (lane == 0 && n_kv > 0) {
-      int issued_k[kStages] = {0}, issued_v[kStages] = {0};
+      int issued_k[L::kStages] = {0}, issued_v[L::kStages] = {0};
       bool q_issued = false, ok = true;
       mbar_expect_tx(bar(L::b_qfull), NT * kTileBytes);
       for (int t = 0; t < NT; ++t)
         for (int half = 0; half < 2; ++half)
           tma_load_4d(sb + L::q_off + t * kTileBytes + half * kBoxBytes, &tm_q, bar(L::b_qfull),
-                      half * 64, h0 + t, pd.q_row0 + i0, b);
+                      half * 64, h0 + t, pd.q_row0 + i0, b);  // packed map: heads h0.., rows 0..
       q_issued = true;
       for (int j = 0; j < n_kv && ok; ++j) {
-        const int st = j % kStages;
-        const int kv_row = pd.kv_row0 + j * kBN;
-        if (j >= kStages && !wait_bar(bar(L::b_kempty + st), ((j / kStages) - 1) & 1, abort_flag)) {
+        const int st = j % L::kStages;
+        const int kv_row = pd.kv_row0 + (int)ks + j * kBN;
+        if (j >= L::kStages && !wait_bar(bar(L::b_kempty + st), ((j / L::kStages) - 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -330,7 +348,7 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
           tma_load_4d(sb + L::k_off + st * kTileBytes + half * kBoxBytes, &tm_k,
                       bar(L::b_kfull + st), half * 64, hk, kv_row, b);
         ++issued_k[st];
-        if (j >= kStages && !wait_bar(bar(L::b_vempty + st), ((j / kStages) - 1) & 1, abort_flag)) {
+        if (j >= L::kStages && !wait_bar(bar(L::b_vempty + st), ((j / L::kStages) - 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -343,7 +361,7 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
       if (!ok) {
         // Let the copies already in flight land before the CTA exits.
         if (q_issued) wait_bar(bar(L::b_qfull), 0, abort_flag, false);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < L::kStages; ++s) {
           if (issued_k[s] > 0) wait_bar(bar(L::b_kfull + s), (issued_k[s] - 1) & 1, abort_flag, false);
           if (issued_v[s] > 0) wait_bar(bar(L::b_vfull + s), (issued_v[s] - 1) & 1, abort_flag, false);
         }
@@ -398,12 +416,12 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
         mma_commit(bar(L::b_kempty + 0));
       }
       for (int j = 0; j < n_kv && ok; ++j) {
-        const int st = j % kStages;
-        const int st1 = (j + 1) % kStages;
+        const int st = j % L::kStages;
+        const int st1 = (j + 1) % L::kStages;
         const bool more = j + 1 < n_kv;
         for (int t = 0; t < NT && ok; ++t) {
           // Each wait sits right before the first MMA that needs it.
-          if ((t == 0 && !wait_bar(bar(L::b_vfull + st), (j / kStages) & 1, abort_flag)) ||
+          if ((t == 0 && !wait_bar(bar(L::b_vfull + st), (j / L::kStages) & 1, abort_flag)) ||
               !wait_bar(bar(L::b_pready + t), j & 1, abort_flag)) {
             ok = false;
             break;
@@ -413,7 +431,7 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
           if (t == NT - 1) mma_commit(bar(L::b_vempty + st));
           if (kStrictOrder || !more) mma_commit(bar(L::b_pvdone + t));
           if (more) {
-            if (t == 0 && !wait_bar(bar(L::b_kfull + st1), ((j + 1) / kStages) & 1, abort_flag)) {
+            if (t == 0 && !wait_bar(bar(L::b_kfull + st1), ((j + 1) / L::kStages) & 1, abort_flag)) {
               ok = false;
               break;
             }
@@ -441,9 +459,13 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t t_s = tmem + lane_off + t * 128;
     const uint32_t t_o = tmem + lane_off + (NT + t) * 128;
-    int64_t lim = pd.kv_len;  // this row's visible keys: [0, lim)
+    // Query row (inside the pair's chunk) and head of this tile row.
+    const int qrow = G == 0 ? i0 + r : r / G;
+    const int head = G == 0 ? h0 + t : h0 + r % G;
+    const bool valid = G == 0 ? r < q_rows : qrow < q_rows;
+    int64_t lim = ke;  // this row's visible keys: [ks, lim)
     if (p.causal) {
-      const int64_t c = (int64_t)(i0 + r) + pd.delta + 1;
+      const int64_t c = (int64_t)qrow + pd.delta + 1;
       lim = c < lim ? c : lim;
     }
     const float sl2 = p.scale_log2;
@@ -462,7 +484,7 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kBN; ++c) s[c] = __uint_as_float(sr[c]);
       if (j >= n_unmasked) {
-        int64_t nv = lim - (int64_t)j * kBN;
+        int64_t nv = lim - ks - (int64_t)j * kBN;
         const int nvis = nv < 0 ? 0 : (nv > kBN ? kBN : (int)nv);
 #pragma unroll
         for (int c = 0; c < kBN; ++c)
@@ -534,11 +556,10 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
       tc_fence_after();
     }
     if (__all_sync(0xffffffffu, ok && !*abort_flag)) {
-      const bool valid = r < q_rows;
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       RowSink sink;
-      if (valid) sink.init(p, pd, b, h0 + t, i0 + r, lse, true);
+      if (valid) sink.init(p, pd, b, head, qrow, lse, true, G == 0 ? -1 : pd.slot + split);
 #pragma unroll 1
       for (int cc = 0; cc < kD / 32; ++cc) {
         float ov[32];
@@ -583,15 +604,16 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// [b, s, h, d] bf16 view -> 4-D tensor map (d, h, s, b), box 64 x 1 x 128 x 1.
+// [b, s, h, d] bf16 view -> 4-D tensor map (d, h, s, b), box 64 x box_h x box_s x 1
+// (box_h * box_s = 128 rows of 128 bytes each).
 bool make_map(CUtensorMap *map, const void *base, int64_t B, int64_t S, int64_t H, int64_t D,
-              int64_t sb, int64_t ss, int64_t sh) {
+              int64_t sb, int64_t ss, int64_t sh, uint32_t box_h = 1, uint32_t box_s = 128) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
   if (B == 1) sb = S * ss > 0 ? S * ss : 8;  // unused extent: any legal stride
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)sh * 2, (cuuint64_t)ss * 2, (cuuint64_t)sb * 2};
-  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t box[4] = {64, box_h, box_s, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -605,14 +627,22 @@ cudaError_t launch_nt(AttnParams &p, cudaStream_t stream) {
   int total = 0;
   for (int x = 0; x < p.n_pairs; ++x) {
     PairDesc &pd = p.pairs[x];
-    pd.n_qtiles = (pd.q_len + kBM - 1) / kBM;
-    pd.cta_begin = total;
-    total += pd.n_qtiles * (p.Hq / NT) * p.B;
+    if (p.pack_g > 0) {  // n_qtiles counts kv splits in packed mode
+      pd.n_qtiles = (pd.kv_len + p.kv_split - 1) / p.kv_split;
+      pd.cta_begin = total;
+      total += pd.n_qtiles * p.Hkv * p.B;
+    } else {
+      pd.n_qtiles = (pd.q_len + kBM - 1) / kBM;
+      pd.cta_begin = total;
+      total += pd.n_qtiles * (p.Hq / NT) * p.B;
+    }
   }
   p.total_ctas = total;
   if (total == 0) return cudaSuccess;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.q, p.B, p.q_rows_total, p.Hq, kD, p.q_sb, p.q_ss, p.q_sh) ||
+  const uint32_t qbox_h = p.pack_g > 0 ? (uint32_t)p.pack_g : 1u;
+  const uint32_t qbox_s = p.pack_g > 0 ? (uint32_t)(kBM / p.pack_g) : (uint32_t)kBM;
+  if (!make_map(&mq, p.q, p.B, p.q_rows_total, p.Hq, kD, p.q_sb, p.q_ss, p.q_sh, qbox_h, qbox_s) ||
       !make_map(&mk, p.k, p.B, p.kv_rows_total, p.Hkv, kD, p.k_sb, p.k_ss, p.k_sh) ||
       !make_map(&mv, p.v, p.B, p.kv_rows_total, p.Hkv, kD, p.v_sb, p.v_ss, p.v_sh))
     return cudaErrorInvalidValue;
@@ -633,7 +663,16 @@ cudaError_t launch_nt(AttnParams &p, cudaStream_t stream) {
 }  // namespace
 
 bool attn_tc_supported(const AttnParams &p) {
-  return !p.in_f32 && p.D == kD && p.q_rows_total > 0 && p.kv_rows_total > 0;
+  if (p.in_f32 || p.D != kD || p.q_rows_total <= 0 || p.kv_rows_total <= 0) return false;
+  if (p.pack_g > 0) {
+    // Packed decode tiles: the group fills whole TMA boxes and every query
+    // row of a pair fits in one 128-row tile; splits are whole KV tiles.
+    if (p.pack_g != p.Hq / p.Hkv || kBM % p.pack_g != 0 || p.kv_split <= 0 || p.kv_split % kBN)
+      return false;
+    for (int x = 0; x < p.n_pairs; ++x)
+      if (p.pairs[x].q_len > kBM / p.pack_g) return false;
+  }
+  return true;
 }
 
 // CPATTN_STRICT_MMA_ORDER=1 selects the schedule that waits for each PV MMA
@@ -646,7 +685,8 @@ bool strict_mma_order() {
 cudaError_t launch_attn_tc(AttnParams &p, cudaStream_t stream) {
   const int g = p.Hq / p.Hkv;
   const bool strict = strict_mma_order();
-  if (g % 2 == 0) return strict ? launch_nt<2, true>(p, stream) : launch_nt<2, false>(p, stream);
+  if (p.pack_g == 0 && g % 2 == 0)
+    return strict ? launch_nt<2, true>(p, stream) : launch_nt<2, false>(p, stream);
   return strict ? launch_nt<1, true>(p, stream) : launch_nt<1, false>(p, stream);
 }
 

@@ -54,6 +54,13 @@ struct AttnParams {
   int64_t q_rows_total, kv_rows_total;  // s extent of the q and k/v tensors
   int32_t in_f32;           // inputs are fp32 (else bf16)
   int32_t total_ctas;       // filled by the launcher
+  // Decode layout (tensor-core kernel only): pack_g > 0 packs the pack_g
+  // query heads that share a kv head, for up to 128 / pack_g query rows, into
+  // one 128-row tile (tile row r = row r / pack_g, head hk * pack_g + r % pack_g),
+  // and each CTA takes kv_split keys of its pair, writing an fp32 partial to
+  // slot pairs[x].slot + split.  pack_g = 0: one head per tile row block.
+  int32_t pack_g;
+  int32_t kv_split;
   OutView out;              // final output (absolute q rows)
   OutView acc;              // Pass-KV fp32 accumulator (absolute q rows)
   OutView part;             // Pass-Q slot 0 (chunk-relative rows)

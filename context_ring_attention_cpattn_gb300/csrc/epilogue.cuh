@@ -113,8 +113,9 @@ struct RowSink {
   // rel_row: row inside the pair's q chunk.  lse_p: the partial's LSE.
   // write_lse: this thread writes the LSE (one thread per row and head).
   __device__ __forceinline__ void init(const AttnParams &p, const PairDesc &pd, int b, int h,
-                                       int rel_row, float lse_p, bool write_lse) {
+                                       int rel_row, float lse_p, bool write_lse, int slot = -1) {
     mode = pd.mode;
+    if (slot < 0) slot = pd.slot;
     const int64_t abs_row = (int64_t)pd.q_row0 + rel_row;
     acc = nullptr;
     wa = 0.f;
@@ -125,8 +126,8 @@ struct RowSink {
       if (write_lse) *view_lse(p.out, b, abs_row, h) = lse_p;
     } else if (mode == kPartial) {
       OutView w = p.part;
-      w.o = reinterpret_cast<float *>(w.o) + (int64_t)pd.slot * p.part_o_stride;
-      w.lse = w.lse + (int64_t)pd.slot * p.part_lse_stride;
+      w.o = reinterpret_cast<float *>(w.o) + (int64_t)slot * p.part_o_stride;
+      w.lse = w.lse + (int64_t)slot * p.part_lse_stride;
       dst = view_row(w, b, rel_row, h);
       dst_f32 = 1;
       if (write_lse) *view_lse(w, b, rel_row, h) = lse_p;

@@ -42,7 +42,7 @@ class Workload:
 
     @property
     def chunk_q(self) -> int:
-        return self.sq // self.n_chunks
+        return self.sq // self.n_chunks if self.sq >= self.n_chunks else self.sq
 
     @property
     def chunk_kv(self) -> int:
@@ -67,6 +67,9 @@ WORKLOADS = {
     "partial-32k": Workload("partial-32k", 1, 16, 1, 128, 2048, 32768, 30720, 8, "bf16"),
     "128k": Workload("128k", 1, 16, 1, 128, 131072, 131072, 0, 16, "bf16"),
     "1m": Workload("1m", 1, 8, 1, 128, 1048576, 1048576, 0, 8, "bf16"),
+    # Decode-shaped Pass-Q: one new token per sequence against a 128K-token
+    # cache sharded over 16 CP ranks, 8 sequences (405B TP-8 shard heads).
+    "decode-128k-b8": Workload("decode-128k-b8", 8, 16, 1, 128, 1, 131072, 131071, 16, "bf16"),
 }
 
 

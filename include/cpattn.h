@@ -142,6 +142,32 @@ cpattn_status cpattn_prefill(const cpattn_tensor *q, const cpattn_tensor *k,
                              void *stream);
 
 /*
+ * cpattn_decode -- Pass-Q for decode-shaped queries: a few new tokens attend
+ * to a long KV cache sharded over n_chunks emulated CP ranks (article's CP
+ * section, Pass-Q bullet: query tensors are passed among the ranks while K/V
+ * stay; the reading notes' framing that decode is memory-bound and prefill
+ * compute-bound, section "The communication bottleneck across all three
+ * axes").  Each rank's chunk is split further into pieces of whole 128-key
+ * tiles so that every SM streams K/V; each piece yields an fp32 partial and
+ * all partials are merged by LSE in ascending (chunk, piece) order.
+ *
+ *   q      [b, n_tok, hq, d]   token i at absolute position q_base + i
+ *   k, v   [b, skv, hkv, d]    the cache; key row j at position j
+ *   o, lse as for cpattn_prefill ([b, n_tok, hq, d], [b, hq, n_tok])
+ *   n_chunks 1..64 dividing skv; workspace >= cpattn_decode_workspace_size
+ * bf16 with d = 128 and n_tok * (hq / hkv) <= 128 (hq / hkv dividing 128)
+ * packs all query heads of a kv head into one tensor-core tile; other shapes
+ * run one tile per head (or the fp32/d=64 kernel) with one piece per chunk.
+ */
+cpattn_status cpattn_decode_workspace_size(const cpattn_tensor *q, const cpattn_tensor *k,
+                                           int64_t q_base, int n_chunks, int causal,
+                                           size_t *bytes);
+cpattn_status cpattn_decode(const cpattn_tensor *q, const cpattn_tensor *k, const cpattn_tensor *v,
+                            int64_t q_base, int n_chunks, int causal, float scale,
+                            cpattn_tensor *o, float *lse, void *workspace, size_t workspace_bytes,
+                            void *stream);
+
+/*
  * One entry of the host-side ring plan (no GPU needed): at ring `step`, the
  * pair (q_chunk, kv_chunk) is computed and its result routed by `role`.
  */

@@ -214,3 +214,21 @@ def test_plan_reproduces_full_attention(lib, sq, skv, q_base, n, causal, mode):
     assert np.array_equal(np.isneginf(lse), np.isneginf(ref_l))
     fin = np.isfinite(ref_l)
     np.testing.assert_allclose(lse[fin], ref_l[fin], rtol=0, atol=1e-12)
+
+
+def test_decode_workspace_sizes(lib):
+    size = ctypes.c_size_t()
+    # One token at the end of a 131072-key cache, 16 q heads on 1 kv head, 16 chunks:
+    # pieces of 256 keys (total keys / 1024 CTAs, at least 256) -> 512 fp32 partials.
+    q, k = T(s=1, h=16), T(s=131072, h=1)
+    assert lib.cpattn_decode_workspace_size(ctypes.byref(q), ctypes.byref(k), 131071, 16, 1,
+                                            ctypes.byref(size)) == 0
+    align = lambda x: (x + 255) // 256 * 256
+    assert size.value == align(512 * 16 * 128 * 4) + align(512 * 16 * 4)
+    # A token at position 1000 sees only the first chunk's first 1001 keys: 4 pieces.
+    assert lib.cpattn_decode_workspace_size(ctypes.byref(q), ctypes.byref(k), 1000, 16, 1,
+                                            ctypes.byref(size)) == 0
+    assert size.value == align(4 * 16 * 128 * 4) + align(4 * 16 * 4)
+    # n_chunks must divide the cache length.
+    assert lib.cpattn_decode_workspace_size(ctypes.byref(q), ctypes.byref(k), 0, 3, 1,
+                                            ctypes.byref(size)) == INVALID
