@@ -28,7 +28,19 @@ class CpattnTensor(ctypes.Structure):
 
 class PlanEntry(ctypes.Structure):
     _fields_ = [("step", ctypes.c_int32), ("q_chunk", ctypes.c_int32),
-                ("kv_chunk", ctypes.c_int32), ("role", ctypes.c_int32), ("slot", ctypes.c_int32)]
+                ("kv_chunk", ctypes.c_int32), ("role", ctypes.c_int32), ("slot", ctypes.c_int32),
+                ("launch", ctypes.c_int32), ("rank", ctypes.c_int32)]
+
+
+class PrefillOptions(ctypes.Structure):
+    _fields_ = [("assignment", ctypes.c_int32), ("reserved", ctypes.c_int32 * 7)]
+
+
+ASSIGN_CONTIGUOUS, ASSIGN_ZIGZAG = 0, 1
+
+
+def _opts(assignment: int):
+    return ctypes.byref(PrefillOptions(int(assignment)))
 
 
 class ProfileRecord(ctypes.Structure):
@@ -38,6 +50,8 @@ class ProfileRecord(ctypes.Structure):
 EXPORTED = ["cpattn_partial", "cpattn_merge", "cpattn_prefill_workspace_size", "cpattn_prefill",
             "cpattn_prefill_plan", "cpattn_prefill_host_scratch_size", "cpattn_prefill_host",
             "cpattn_prefill_noalloc", "cpattn_decode_workspace_size", "cpattn_decode",
+            "cpattn_prefill_ex", "cpattn_prefill_workspace_size_ex", "cpattn_prefill_plan_ex",
+            "cpattn_prefill_critical_path",
             "cpattn_status_string", "cpattn_device_status",
             "cpattn_profile_begin", "cpattn_profile_end"]
 
@@ -78,6 +92,14 @@ def lib():
                                       vp]
     L.cpattn_prefill_noalloc.argtypes = [T, T, T, i64, i32, i32, i32, f32, T, vp, vp]
     L.cpattn_decode_workspace_size.argtypes = [T, T, i64, i32, i32, sz]
+    O = ctypes.POINTER(PrefillOptions)
+    dp = ctypes.POINTER(ctypes.c_double)
+    L.cpattn_prefill_ex.argtypes = [T, T, T, i64, i32, i32, i32, f32, T, vp, vp, ctypes.c_size_t, O,
+                                    vp]
+    L.cpattn_prefill_workspace_size_ex.argtypes = [T, T, i64, i32, i32, i32, O, sz]
+    L.cpattn_prefill_plan_ex.argtypes = [i64, i64, i64, i32, i32, i32, O, ctypes.POINTER(PlanEntry),
+                                         i32, ctypes.POINTER(ctypes.c_int)]
+    L.cpattn_prefill_critical_path.argtypes = [i64, i64, i64, i32, i32, i32, O, dp, dp, dp]
     L.cpattn_decode.argtypes = [T, T, T, i64, i32, i32, f32, T, vp, vp, ctypes.c_size_t, vp]
     L.cpattn_status_string.argtypes = [i32]
     L.cpattn_status_string.restype = ctypes.c_char_p
@@ -150,18 +172,21 @@ def merge_(o_a, lse_a, o_b, lse_b, stream=None):
     return o_a, lse_a
 
 
-def workspace_size(q, k, n_chunks: int, mode: int, q_base: int = 0, causal: bool = True) -> int:
+def workspace_size(q, k, n_chunks: int, mode: int, q_base: int = 0, causal: bool = True,
+                   assignment: int = ASSIGN_CONTIGUOUS) -> int:
     n = ctypes.c_size_t(0)
     qv, kv_ = view(q), view(k)
-    _check(lib().cpattn_prefill_workspace_size(ctypes.byref(qv), ctypes.byref(kv_), int(q_base),
-                                               int(n_chunks), int(mode), int(bool(causal)),
-                                               ctypes.byref(n)), "cpattn_prefill_workspace_size")
+    _check(lib().cpattn_prefill_workspace_size_ex(ctypes.byref(qv), ctypes.byref(kv_), int(q_base),
+                                                  int(n_chunks), int(mode), int(bool(causal)),
+                                                  _opts(assignment), ctypes.byref(n)),
+           "cpattn_prefill_workspace_size_ex")
     return n.value
 
 
 def prefill(q, k, v, n_chunks: int, mode: int, q_base: int = 0, causal: bool = True, scale=None,
-            out=None, lse=None, workspace=None, out_dtype=None, stream=None):
-    """CP prefill of one attention layer on one GPU; see cpattn_prefill."""
+            out=None, lse=None, workspace=None, out_dtype=None, stream=None,
+            assignment: int = ASSIGN_CONTIGUOUS):
+    """CP prefill of one attention layer on one GPU; see cpattn_prefill_ex."""
     import torch
 
     B, S, H, D = q.shape
@@ -169,16 +194,16 @@ def prefill(q, k, v, n_chunks: int, mode: int, q_base: int = 0, causal: bool = T
         out = torch.empty((B, S, H, D), dtype=out_dtype or q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-    need = workspace_size(q, k, n_chunks, mode, q_base, causal)
+    need = workspace_size(q, k, n_chunks, mode, q_base, causal, assignment)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     qv, kv_, vv, ov = view(q), view(k), view(v), view(out)
-    _check(lib().cpattn_prefill(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
-                                int(q_base), int(n_chunks), int(mode), int(bool(causal)),
-                                float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(), ws_ptr,
-                                ws_len, _stream(stream)), "cpattn_prefill")
+    _check(lib().cpattn_prefill_ex(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
+                                   int(q_base), int(n_chunks), int(mode), int(bool(causal)),
+                                   float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(), ws_ptr,
+                                   ws_len, _opts(assignment), _stream(stream)), "cpattn_prefill_ex")
     return out, lse
 
 
@@ -258,17 +283,34 @@ def prefill_host(q, k, v, n_chunks, mode, out, lse, dev_scratch, q_base=0, causa
 
 
 def prefill_plan(sq: int, skv: int, n_chunks: int, mode: int, q_base: int = 0,
-                 causal: bool = True):
-    """Launch-order list of (step, q_chunk, kv_chunk, role, slot) (host only)."""
+                 causal: bool = True, assignment: int = ASSIGN_CONTIGUOUS, full: bool = False):
+    """Launch-order list of (step, q_piece, kv_piece, role, slot) -- plus
+    (launch, rank) when full=True -- computed on the host."""
     n = ctypes.c_int(0)
-    _check(lib().cpattn_prefill_plan(int(sq), int(skv), int(q_base), int(n_chunks), int(mode),
-                                     int(bool(causal)), None, 0, ctypes.byref(n)),
-           "cpattn_prefill_plan")
+    _check(lib().cpattn_prefill_plan_ex(int(sq), int(skv), int(q_base), int(n_chunks), int(mode),
+                                        int(bool(causal)), _opts(assignment), None, 0,
+                                        ctypes.byref(n)), "cpattn_prefill_plan_ex")
     arr = (PlanEntry * max(1, n.value))()
-    _check(lib().cpattn_prefill_plan(int(sq), int(skv), int(q_base), int(n_chunks), int(mode),
-                                     int(bool(causal)), arr, n.value, ctypes.byref(n)),
-           "cpattn_prefill_plan")
+    _check(lib().cpattn_prefill_plan_ex(int(sq), int(skv), int(q_base), int(n_chunks), int(mode),
+                                        int(bool(causal)), _opts(assignment), arr, n.value,
+                                        ctypes.byref(n)), "cpattn_prefill_plan_ex")
+    if full:
+        return [(e.step, e.q_chunk, e.kv_chunk, e.role, e.slot, e.launch, e.rank)
+                for e in arr[:n.value]]
     return [(e.step, e.q_chunk, e.kv_chunk, e.role, e.slot) for e in arr[:n.value]]
+
+
+def critical_path(sq: int, skv: int, n_chunks: int, mode: int, q_base: int = 0,
+                  causal: bool = True, assignment: int = ASSIGN_CONTIGUOUS):
+    """(critical, total, per-step maxima) of the emulated ring, in visible
+    (query, key) pairs per (batch, head); see cpattn_prefill_critical_path."""
+    crit, tot = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    steps = (ctypes.c_double * n_chunks)()
+    _check(lib().cpattn_prefill_critical_path(int(sq), int(skv), int(q_base), int(n_chunks),
+                                              int(mode), int(bool(causal)), _opts(assignment),
+                                              steps, ctypes.byref(crit), ctypes.byref(tot)),
+           "cpattn_prefill_critical_path")
+    return crit.value, tot.value, list(steps)
 
 
 def device_status(clear: bool = True) -> int:

@@ -148,16 +148,32 @@ void prof_after(cudaStream_t st, int kind, double work) {
 }
 
 // ----------------------------------------------------------------- the plan
+// The sequence is cut into pieces; rank r of N holds piece r (contiguous
+// assignment) or pieces r and 2N-1-r (zigzag assignment, which gives every
+// rank the same causal work).  Q and K/V use the same assignment.
 struct Plan {
   int N = 0;
   int mode = 0;
-  int64_t Cq = 0, C = 0;
+  int assign = CPATTN_ASSIGN_CONTIGUOUS;
+  int P = 0;                               // pieces per sequence
+  int64_t Cq = 0, C = 0;                   // Q and K/V piece lengths
   std::vector<cpattn_plan_entry> entries;  // launch order
-  std::vector<int> count;                  // non-empty pairs per Q chunk
-  std::vector<int> slot0;                  // Pass-Q: first slot of the chunk (-1: none)
+  int n_launches = 0;
+  std::vector<int> count;                  // visible K/V pieces per Q piece
+  std::vector<int> slot0;                  // Pass-Q: first slot of the Q piece (-1: none)
   int n_slots = 0;
   bool need_acc = false;                   // Pass-KV needs the accumulator
 };
+
+int rank_pieces(const Plan &pl, int r, int out[2]) {
+  if (pl.assign == CPATTN_ASSIGN_ZIGZAG) {
+    out[0] = r;
+    out[1] = 2 * pl.N - 1 - r;
+    return 2;
+  }
+  out[0] = r;
+  return 1;
+}
 
 bool pair_visible(const Plan &pl, int64_t q_base, bool causal, int i, int j) {
   if (pl.Cq <= 0 || pl.C <= 0) return false;
@@ -166,59 +182,115 @@ bool pair_visible(const Plan &pl, int64_t q_base, bool causal, int i, int j) {
 }
 
 cpattn_status build_plan(int64_t sq, int64_t skv, int64_t q_base, int n_chunks, int mode,
-                         int causal, Plan &pl) {
+                         int causal, int assign, Plan &pl) {
   if (n_chunks < 1 || n_chunks > kMaxPairs) return CPATTN_ERR_INVALID_ARG;
   if (mode != CPATTN_PASS_KV && mode != CPATTN_PASS_Q) return CPATTN_ERR_INVALID_ARG;
-  if (sq < 0 || skv < 0 || sq % n_chunks != 0 || skv % n_chunks != 0) return CPATTN_ERR_INVALID_ARG;
+  if (assign != CPATTN_ASSIGN_CONTIGUOUS && assign != CPATTN_ASSIGN_ZIGZAG)
+    return CPATTN_ERR_INVALID_ARG;
+  const int P = assign == CPATTN_ASSIGN_ZIGZAG ? 2 * n_chunks : n_chunks;
+  if (sq < 0 || skv < 0 || sq % P != 0 || skv % P != 0) return CPATTN_ERR_INVALID_ARG;
   if (sq > kMaxRows || skv > kMaxRows || q_base < -kMaxRows * 4 || q_base > kMaxRows * 4)
     return CPATTN_ERR_UNSUPPORTED;
+  // Pairs per launch: N (contiguous), 2N (zigzag Pass-KV), 4N (zigzag Pass-Q).
+  const int per_launch = assign == CPATTN_ASSIGN_ZIGZAG ? (mode == CPATTN_PASS_Q ? 4 : 2) : 1;
+  if (per_launch * n_chunks > kMaxPairs) return CPATTN_ERR_UNSUPPORTED;
   const int N = n_chunks;
   pl.N = N;
   pl.mode = mode;
-  pl.Cq = sq / N;
-  pl.C = skv / N;
-  pl.count.assign(N, 0);
-  pl.slot0.assign(N, -1);
+  pl.assign = assign;
+  pl.P = P;
+  pl.Cq = sq / P;
+  pl.C = skv / P;
+  pl.count.assign(P, 0);
+  pl.slot0.assign(P, -1);
   pl.entries.clear();
-  for (int i = 0; i < N; ++i)
-    for (int j = 0; j < N; ++j) pl.count[i] += pair_visible(pl, q_base, causal, i, j) ? 1 : 0;
+  for (int i = 0; i < P; ++i)
+    for (int j = 0; j < P; ++j) pl.count[i] += pair_visible(pl, q_base, causal, i, j) ? 1 : 0;
   pl.n_slots = 0;
   if (mode == CPATTN_PASS_Q) {
-    for (int i = 0; i < N; ++i)
+    for (int i = 0; i < P; ++i)
       if (pl.count[i] >= 2) {
         pl.slot0[i] = pl.n_slots;
         pl.n_slots += pl.count[i];
       }
   }
-  std::vector<int> seen(N, 0);
+  std::vector<int> seen(P, 0);
+  int launch = 0;
+  auto emit = [&](int t, int r, int i, int j) {
+    if (!pair_visible(pl, q_base, causal, i, j)) return;
+    cpattn_plan_entry e;
+    e.step = t;
+    e.q_chunk = i;
+    e.kv_chunk = j;
+    e.slot = -1;
+    e.launch = launch;
+    e.rank = r;
+    if (pl.count[i] == 1) {
+      e.role = CPATTN_ROLE_STORE;
+    } else if (mode == CPATTN_PASS_KV) {
+      const int k = seen[i]++;
+      e.role = k == 0 ? CPATTN_ROLE_ACC_INIT
+                      : (k == pl.count[i] - 1 ? CPATTN_ROLE_ACC_FINAL : CPATTN_ROLE_ACC_MERGE);
+      pl.need_acc = true;
+    } else {
+      int rank = 0;  // position of j among piece i's visible K/V pieces, ascending
+      for (int jj = 0; jj < j; ++jj) rank += pair_visible(pl, q_base, causal, i, jj) ? 1 : 0;
+      e.role = CPATTN_ROLE_PARTIAL;
+      e.slot = pl.slot0[i] + rank;
+    }
+    pl.entries.push_back(e);
+  };
   for (int t = 0; t < N; ++t) {
-    for (int r = 0; r < N; ++r) {
-      const int i = mode == CPATTN_PASS_KV ? r : ((r - t) % N + N) % N;
-      const int j = mode == CPATTN_PASS_KV ? ((r - t) % N + N) % N : r;
-      if (!pair_visible(pl, q_base, causal, i, j)) continue;
-      cpattn_plan_entry e;
-      e.step = t;
-      e.q_chunk = i;
-      e.kv_chunk = j;
-      e.slot = -1;
-      if (pl.count[i] == 1) {
-        e.role = CPATTN_ROLE_STORE;
-      } else if (mode == CPATTN_PASS_KV) {
-        const int k = seen[i]++;
-        e.role = k == 0 ? CPATTN_ROLE_ACC_INIT
-                        : (k == pl.count[i] - 1 ? CPATTN_ROLE_ACC_FINAL : CPATTN_ROLE_ACC_MERGE);
-        pl.need_acc = true;
-      } else {
-        // Rank of j among chunk i's visible KV chunks, ascending.
-        int rank = 0;
-        for (int jj = 0; jj < j; ++jj) rank += pair_visible(pl, q_base, causal, i, jj) ? 1 : 0;
-        e.role = CPATTN_ROLE_PARTIAL;
-        e.slot = pl.slot0[i] + rank;
+    if (mode == CPATTN_PASS_KV) {
+      // Rank r keeps its Q pieces and receives the K/V pieces of rank
+      // (r - t) mod N.  Each K/V piece of the visiting rank is its own launch,
+      // so no Q piece's accumulator is updated twice in one launch.
+      const int n_sub = assign == CPATTN_ASSIGN_ZIGZAG ? 2 : 1;
+      for (int u = 0; u < n_sub; ++u) {
+        const size_t before = pl.entries.size();
+        for (int r = 0; r < N; ++r) {
+          int qp[2], kp[2];
+          const int nq = rank_pieces(pl, r, qp);
+          rank_pieces(pl, ((r - t) % N + N) % N, kp);
+          for (int a = 0; a < nq; ++a) emit(t, r, qp[a], kp[u]);
+        }
+        if (pl.entries.size() > before) ++launch;
       }
-      pl.entries.push_back(e);
+    } else {
+      // Rank r keeps its K/V pieces and receives the Q pieces of rank (r - t) mod N.
+      const size_t before = pl.entries.size();
+      for (int r = 0; r < N; ++r) {
+        int qp[2], kp[2];
+        const int nq = rank_pieces(pl, ((r - t) % N + N) % N, qp);
+        const int nk = rank_pieces(pl, r, kp);
+        for (int a = 0; a < nq; ++a)
+          for (int b = 0; b < nk; ++b) emit(t, r, qp[a], kp[b]);
+      }
+      if (pl.entries.size() > before) ++launch;
     }
   }
+  pl.n_launches = launch;
   return CPATTN_OK;
+}
+
+// Work of every (ring step, rank) in visible (query, key) pairs per head:
+// a real ring step lasts as long as its busiest rank.
+void plan_work(const Plan &pl, int64_t q_base, bool causal, std::vector<double> &step_max,
+               double &critical, double &total) {
+  std::vector<double> w((size_t)pl.N * pl.N, 0.0);
+  total = 0.0;
+  for (const auto &e : pl.entries) {
+    const double v = visible_pairs(q_base + (int64_t)e.q_chunk * pl.Cq, pl.Cq,
+                                   (int64_t)e.kv_chunk * pl.C, pl.C, causal);
+    w[(size_t)e.step * pl.N + e.rank] += v;
+    total += v;
+  }
+  step_max.assign(pl.N, 0.0);
+  critical = 0.0;
+  for (int t = 0; t < pl.N; ++t) {
+    for (int r = 0; r < pl.N; ++r) step_max[t] = std::max(step_max[t], w[(size_t)t * pl.N + r]);
+    critical += step_max[t];
+  }
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -265,15 +337,21 @@ cudaError_t launch_attn(AttnParams &p, cudaStream_t st, const cpattn_tensor *q) 
   return e;
 }
 
+int assignment_of(const cpattn_prefill_options *opts) {
+  return opts ? opts->assignment : CPATTN_ASSIGN_CONTIGUOUS;
+}
+
 cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const cpattn_tensor *v,
                            int64_t q_base, int n_chunks, int mode, int causal, float scale,
                            cpattn_tensor *o, float *lse, void *workspace, size_t ws_bytes,
-                           cudaStream_t st) {
+                           const cpattn_prefill_options *opts, cudaStream_t st) {
   cpattn_status s = check_qkv(q, k, v);
   if (s != CPATTN_OK) return s;
   if ((s = check_out(o, lse, q)) != CPATTN_OK) return s;
   Plan pl;
-  if ((s = build_plan(q->s, k->s, q_base, n_chunks, mode, causal, pl)) != CPATTN_OK) return s;
+  if ((s = build_plan(q->s, k->s, q_base, n_chunks, mode, causal, assignment_of(opts), pl)) !=
+      CPATTN_OK)
+    return s;
   const WsLayout wl = ws_layout(pl, q->b, q->s, q->h, q->d);
   if (wl.total > 0) {
     if (workspace == nullptr || ws_bytes < wl.total) return CPATTN_ERR_WORKSPACE;
@@ -308,11 +386,12 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
     p.part_lse_stride = wl.slot_lse_elems;
   }
 
-  // One launch per ring step; pairs ordered by work, largest first.
+  // One launch per ring step (two per step for zigzag Pass-KV, one per
+  // visiting K/V piece); pairs ordered by work, largest first.
   size_t e0 = 0;
-  for (int t = 0; t < pl.N; ++t) {
+  for (int l = 0; l < pl.n_launches; ++l) {
     size_t e1 = e0;
-    while (e1 < pl.entries.size() && pl.entries[e1].step == t) ++e1;
+    while (e1 < pl.entries.size() && pl.entries[e1].launch == l) ++e1;
     if (e1 == e0) continue;
     struct Item { PairDesc pd; double work; };
     std::vector<Item> items;
@@ -353,8 +432,8 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
   const double row_bytes = (double)q->b * pl.Cq * q->h * (q->d * 4.0 + 4.0);
   const double out_bytes = (double)q->b * pl.Cq * q->h * (q->d * elem_bytes(o->dtype) + 4.0);
   // Items with the most partials first (longest CTAs first).
-  std::vector<int> order(pl.N);
-  for (int i = 0; i < pl.N; ++i) order[i] = i;
+  std::vector<int> order(pl.P);
+  for (int i = 0; i < pl.P; ++i) order[i] = i;
   std::stable_sort(order.begin(), order.end(),
                    [&](int a, int b) { return pl.count[a] > pl.count[b]; });
   for (int i : order) {
@@ -533,13 +612,21 @@ cpattn_status cpattn_merge(cpattn_tensor *o_a, float *lse_a, const cpattn_tensor
 cpattn_status cpattn_prefill_workspace_size(const cpattn_tensor *q, const cpattn_tensor *k,
                                             int64_t q_base, int n_chunks, int mode, int causal,
                                             size_t *bytes) {
+  return cpattn_prefill_workspace_size_ex(q, k, q_base, n_chunks, mode, causal, nullptr, bytes);
+}
+
+cpattn_status cpattn_prefill_workspace_size_ex(const cpattn_tensor *q, const cpattn_tensor *k,
+                                               int64_t q_base, int n_chunks, int mode, int causal,
+                                               const cpattn_prefill_options *opts, size_t *bytes) {
   try {
     if (bytes == nullptr) return CPATTN_ERR_INVALID_ARG;
     cpattn_status s = check_view(q);
     if (s != CPATTN_OK) return s;
     if ((s = check_view(k)) != CPATTN_OK) return s;
     Plan pl;
-    if ((s = build_plan(q->s, k->s, q_base, n_chunks, mode, causal, pl)) != CPATTN_OK) return s;
+    if ((s = build_plan(q->s, k->s, q_base, n_chunks, mode, causal, assignment_of(opts), pl)) !=
+        CPATTN_OK)
+      return s;
     *bytes = ws_layout(pl, q->b, q->s, q->h, q->d).total;
     return CPATTN_OK;
   } catch (...) {
@@ -551,9 +638,18 @@ cpattn_status cpattn_prefill(const cpattn_tensor *q, const cpattn_tensor *k,
                              const cpattn_tensor *v, int64_t q_base, int n_chunks, int mode,
                              int causal, float scale, cpattn_tensor *o, float *lse,
                              void *workspace, size_t workspace_bytes, void *stream) {
+  return cpattn_prefill_ex(q, k, v, q_base, n_chunks, mode, causal, scale, o, lse, workspace,
+                           workspace_bytes, nullptr, stream);
+}
+
+cpattn_status cpattn_prefill_ex(const cpattn_tensor *q, const cpattn_tensor *k,
+                                const cpattn_tensor *v, int64_t q_base, int n_chunks, int mode,
+                                int causal, float scale, cpattn_tensor *o, float *lse,
+                                void *workspace, size_t workspace_bytes,
+                                const cpattn_prefill_options *opts, void *stream) {
   try {
     return prefill_impl(q, k, v, q_base, n_chunks, mode, causal, scale, o, lse, workspace,
-                        workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+                        workspace_bytes, opts, reinterpret_cast<cudaStream_t>(stream));
   } catch (...) {
     return CPATTN_ERR_INVALID_ARG;
   }
@@ -655,11 +751,37 @@ cpattn_status cpattn_decode(const cpattn_tensor *q, const cpattn_tensor *k, cons
 cpattn_status cpattn_prefill_plan(int64_t sq, int64_t skv, int64_t q_base, int n_chunks, int mode,
                                   int causal, cpattn_plan_entry *entries, int capacity,
                                   int *n_entries) {
+  return cpattn_prefill_plan_ex(sq, skv, q_base, n_chunks, mode, causal, nullptr, entries,
+                                capacity, n_entries);
+}
+
+cpattn_status cpattn_prefill_critical_path(int64_t sq, int64_t skv, int64_t q_base, int n_chunks,
+                                           int mode, int causal,
+                                           const cpattn_prefill_options *opts,
+                                           double *step_max, double *critical, double *total) {
+  try {
+    if (critical == nullptr || total == nullptr) return CPATTN_ERR_INVALID_ARG;
+    Plan pl;
+    cpattn_status s = build_plan(sq, skv, q_base, n_chunks, mode, causal, assignment_of(opts), pl);
+    if (s != CPATTN_OK) return s;
+    std::vector<double> sm;
+    plan_work(pl, q_base, causal != 0, sm, *critical, *total);
+    if (step_max)
+      for (int t = 0; t < n_chunks; ++t) step_max[t] = sm[t];
+    return CPATTN_OK;
+  } catch (...) {
+    return CPATTN_ERR_INVALID_ARG;
+  }
+}
+
+cpattn_status cpattn_prefill_plan_ex(int64_t sq, int64_t skv, int64_t q_base, int n_chunks,
+                                     int mode, int causal, const cpattn_prefill_options *opts,
+                                     cpattn_plan_entry *entries, int capacity, int *n_entries) {
   try {
     if (n_entries == nullptr || capacity < 0 || (capacity > 0 && entries == nullptr))
       return CPATTN_ERR_INVALID_ARG;
     Plan pl;
-    cpattn_status s = build_plan(sq, skv, q_base, n_chunks, mode, causal, pl);
+    cpattn_status s = build_plan(sq, skv, q_base, n_chunks, mode, causal, assignment_of(opts), pl);
     if (s != CPATTN_OK) return s;
     *n_entries = (int)pl.entries.size();
     for (int x = 0; x < capacity && x < (int)pl.entries.size(); ++x) entries[x] = pl.entries[x];
@@ -717,7 +839,7 @@ cpattn_status cpattn_prefill_host(const cpattn_tensor *q, const cpattn_tensor *k
         cudaMemcpyAsync(dv.data, v->data, tensor_bytes(v), cudaMemcpyHostToDevice, st) != cudaSuccess)
       return CPATTN_ERR_CUDA;
     s = prefill_impl(&dq, &dk, &dv, q_base, n_chunks, mode, causal, scale, &dout, dlse, ws,
-                     ws_bytes, st);
+                     ws_bytes, nullptr, st);
     if (s != CPATTN_OK) return s;
     if (cudaMemcpyAsync(o->data, dout.data, o_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaMemcpyAsync(lse, dlse, lse_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)

@@ -180,7 +180,13 @@ typedef enum {
 } cpattn_role;
 
 typedef struct {
-  int32_t step, q_chunk, kv_chunk, role, slot;
+  int32_t step;      /* ring step t */
+  int32_t q_chunk;   /* Q piece (= chunk for the contiguous assignment) */
+  int32_t kv_chunk;  /* K/V piece */
+  int32_t role;      /* cpattn_role */
+  int32_t slot;      /* CPATTN_ROLE_PARTIAL: workspace slot, else -1 */
+  int32_t launch;    /* index of the kernel launch that computes this pair */
+  int32_t rank;      /* emulated CP rank that computes this pair */
 } cpattn_plan_entry;
 
 /*
@@ -191,6 +197,47 @@ typedef struct {
 cpattn_status cpattn_prefill_plan(int64_t sq, int64_t skv, int64_t q_base, int n_chunks,
                                   int mode, int causal, cpattn_plan_entry *entries,
                                   int capacity, int *n_entries);
+
+/*
+ * Chunk-to-rank assignment (options of the *_ex calls).  With contiguous
+ * chunks the causal work of rank r grows with r, so a real ring waits for
+ * rank N-1 at every step.  CPATTN_ASSIGN_ZIGZAG cuts the sequence into 2N
+ * pieces and gives rank r pieces r and 2N-1-r (the same for Q and K/V), which
+ * evens the causal work out.  The result is the same attention either way.
+ * Zigzag needs sq and skv divisible by 2N and N <= 32 (Pass-KV) or N <= 16
+ * (Pass-Q); Pass-KV then launches once per visiting K/V piece.
+ */
+typedef enum { CPATTN_ASSIGN_CONTIGUOUS = 0, CPATTN_ASSIGN_ZIGZAG = 1 } cpattn_assignment;
+typedef struct {
+  int32_t assignment;   /* cpattn_assignment */
+  int32_t reserved[7];  /* zero */
+} cpattn_prefill_options;
+
+/* cpattn_prefill / _workspace_size / _plan with options (NULL = defaults). */
+cpattn_status cpattn_prefill_ex(const cpattn_tensor *q, const cpattn_tensor *k,
+                                const cpattn_tensor *v, int64_t q_base, int n_chunks, int mode,
+                                int causal, float scale, cpattn_tensor *o, float *lse,
+                                void *workspace, size_t workspace_bytes,
+                                const cpattn_prefill_options *opts, void *stream);
+cpattn_status cpattn_prefill_workspace_size_ex(const cpattn_tensor *q, const cpattn_tensor *k,
+                                               int64_t q_base, int n_chunks, int mode, int causal,
+                                               const cpattn_prefill_options *opts, size_t *bytes);
+cpattn_status cpattn_prefill_plan_ex(int64_t sq, int64_t skv, int64_t q_base, int n_chunks,
+                                     int mode, int causal, const cpattn_prefill_options *opts,
+                                     cpattn_plan_entry *entries, int capacity, int *n_entries);
+
+/*
+ * cpattn_prefill_critical_path -- the ring's critical path on N GPUs, from
+ * the plan (host only): each step lasts as long as its busiest rank, so
+ * *critical = sum over steps of max over ranks of the rank's work, *total =
+ * all work, both in visible (query, key) pairs per (batch, head) (multiply by
+ * 4 * d * hq * b for FLOPs).  step_max (may be NULL) receives the per-step
+ * maxima [n_chunks].  total / (N * critical) is the ring's load balance.
+ */
+cpattn_status cpattn_prefill_critical_path(int64_t sq, int64_t skv, int64_t q_base, int n_chunks,
+                                           int mode, int causal,
+                                           const cpattn_prefill_options *opts,
+                                           double *step_max, double *critical, double *total);
 
 /*
  * cpattn_prefill_host -- end-to-end convenience: q, k, v, o are HOST tensors

@@ -156,12 +156,13 @@ def test_plan_structure(lib, sq, skv, q_base, n, causal, mode):
     assert len(slots) == len(set(slots))
 
 
-def emulate_plan(q, k, v, n, mode, q_base, causal):
+def emulate_plan(q, k, v, n, mode, q_base, causal, assignment=B.ASSIGN_CONTIGUOUS):
     """Run the library's plan on the CPU with oracle partials and merges."""
     Bsz, sq, hq, d = q.shape
     skv = k.shape[1]
-    cq, c = sq // n, skv // n
-    plan = B.prefill_plan(sq, skv, n, mode, q_base, causal)
+    pieces = 2 * n if assignment == B.ASSIGN_ZIGZAG else n
+    cq, c = sq // pieces, skv // pieces
+    plan = B.prefill_plan(sq, skv, n, mode, q_base, causal, assignment)
     out_o = np.full((Bsz, sq, hq, d), np.nan)
     out_l = np.full((Bsz, hq, sq), np.nan)
     acc = {}
@@ -185,7 +186,7 @@ def emulate_plan(q, k, v, n, mode, q_base, causal):
                 out_l[:, :, i * cq:(i + 1) * cq] = np.transpose(ml, (0, 2, 1))
         else:
             slots[slot] = (i, j, o, lse_t)
-    for i in range(n):
+    for i in range(pieces):
         parts = sorted((s, val) for s, val in slots.items() if val[0] == i)
         if parts:
             assert [val[1] for _, val in parts] == sorted(val[1] for _, val in parts)
@@ -232,3 +233,56 @@ def test_decode_workspace_sizes(lib):
     # n_chunks must divide the cache length.
     assert lib.cpattn_decode_workspace_size(ctypes.byref(q), ctypes.byref(k), 0, 3, 1,
                                             ctypes.byref(size)) == INVALID
+
+
+# --------------------------------------------------------------------- zigzag assignment
+@pytest.mark.parametrize("sq,skv,q_base,n,causal", [(256, 256, 0, 4, True), (240, 240, 0, 3, True),
+                                                    (160, 320, 160, 4, True), (128, 128, 0, 2, False)])
+@pytest.mark.parametrize("mode", [B.PASS_KV, B.PASS_Q])
+def test_zigzag_plan_reproduces_full_attention(lib, sq, skv, q_base, n, causal, mode):
+    rng = np.random.default_rng(sq + n)
+    q = rng.standard_normal((1, sq, 2, 8)).astype(np.float32)
+    k = rng.standard_normal((1, skv, 1, 8)).astype(np.float32)
+    v = rng.standard_normal((1, skv, 1, 8)).astype(np.float32)
+    o, lse = emulate_plan(q, k, v, n, mode, q_base, causal, B.ASSIGN_ZIGZAG)
+    ref_o, ref_l = oracle.attention(q, k, v, q_pos=q_base + np.arange(sq), causal=causal)
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_l, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", [B.PASS_KV, B.PASS_Q])
+def test_zigzag_plan_structure(lib, mode):
+    n = 4
+    plan = B.prefill_plan(512, 512, n, mode, 0, True, B.ASSIGN_ZIGZAG, full=True)
+    owner = lambda piece: piece if piece < n else 2 * n - 1 - piece
+    seen = set()
+    for step, qp, kp, role, slot, launch, rank in plan:
+        # Pass-KV: the rank owns the Q piece and receives K/V of rank (r - t) mod n;
+        # Pass-Q: the rank owns the K/V piece and receives Q of rank (r - t) mod n.
+        if mode == B.PASS_KV:
+            assert owner(qp) == rank and owner(kp) == (rank - step) % n
+        else:
+            assert owner(kp) == rank and owner(qp) == (rank - step) % n
+        seen.add((qp, kp))
+    assert seen == {(i, j) for i in range(2 * n) for j in range(2 * n) if j <= i}
+    # No Q piece is written twice by one launch (accumulator updates stay ordered).
+    per_launch = {}
+    for step, qp, kp, role, slot, launch, rank in plan:
+        if role != 4:
+            assert (launch, qp) not in per_launch
+            per_launch[(launch, qp)] = True
+
+
+def test_critical_path_balance(lib):
+    """Contiguous chunks leave the causal ring about half idle (each step waits
+    for the rank with the most visible keys); zigzag pieces balance it."""
+    n, s = 8, 8192
+    for mode in (B.PASS_KV, B.PASS_Q):
+        crit_c, tot_c, _ = B.critical_path(s, s, n, mode, 0, True, B.ASSIGN_CONTIGUOUS)
+        crit_z, tot_z, steps = B.critical_path(s, s, n, mode, 0, True, B.ASSIGN_ZIGZAG)
+        assert tot_c == tot_z == s * (s + 1) / 2
+        c = s // n  # closed form for contiguous chunks: one diagonal step, n-1 full steps
+        assert crit_c == c * (c + 1) / 2 + (n - 1) * c * c
+        assert tot_c / (n * crit_c) < 0.55
+        assert tot_z / (n * crit_z) > 0.98
+        assert len(steps) == n and abs(sum(steps) - crit_z) < 1e-6

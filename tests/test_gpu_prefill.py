@@ -92,3 +92,28 @@ def test_prefill_host_entry_point(B):
                           device="cuda")
     B.prefill_host(qh, kh, vh, w.n_chunks, B.PASS_KV, oh, lh, scratch)
     assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3-8b", "partial-32k", "128k"])
+def test_prefill_zigzag_assignment(B, name):
+    """Zigzag chunk-to-rank assignment (rank r holds pieces r and 2N-1-r) gives
+    the same attention as the contiguous one, for both schedules."""
+    from context_ring_attention_cpattn_gb300.workloads import WORKLOADS, make_qkv, sample_rows
+
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w, device="cuda")
+    tol = TOL[w.dtype]
+    rows = sample_rows(w, n=min(N_SAMPLE, w.sq, 1024))
+    ref_o, ref_l = oracle_rows(q, k, v, rows, q_base=w.q_base, causal=w.causal)
+    base = B.prefill(q, k, v, w.n_chunks, B.PASS_KV, q_base=w.q_base, causal=w.causal)
+    for mode in (B.PASS_KV, B.PASS_Q):
+        o, lse = B.prefill(q, k, v, w.n_chunks, mode, q_base=w.q_base, causal=w.causal,
+                           assignment=B.ASSIGN_ZIGZAG)
+        torch.cuda.synchronize()
+        assert B.device_status() == 0
+        compare(o, lse, rows, ref_o, ref_l, tol, f"zigzag {name} mode {mode}")
+        d_o = (o.float() - base[0].float()).abs().max().item()
+        d_l = (lse - base[1]).abs().max().item()
+        assert d_o <= tol[0] and d_l <= tol[1], (d_o, d_l)
+    del q, k, v, base
+    torch.cuda.empty_cache()
