@@ -435,6 +435,20 @@ def main():
                 "share_of_step": tc_ms / elapsed if elapsed else None}
 
     ms_layer = {names[m]: statistics.median(per_mode[m]) for m in modes}
+    # Load balance of the ring this single GPU emulates: on N GPUs each ring
+    # step lasts as long as its busiest rank.  Projected N-GPU time = measured
+    # single-GPU time x critical / total (communication not included).
+    ring = {}
+    for assign, aname in ((B.ASSIGN_CONTIGUOUS, "contiguous"), (B.ASSIGN_ZIGZAG, "zigzag")):
+        ring[aname] = {}
+        for m in modes:
+            try:
+                crit, tot, _ = B.critical_path(w.sq, w.skv, w.n_chunks, m, w.q_base, w.causal, assign)
+            except B.CpattnError:
+                continue
+            ring[aname][names[m]] = {
+                "balance": tot / (w.n_chunks * crit),
+                "projected_ms_per_layer_on_n_ranks": ms_layer[names[m]] * crit / tot}
     hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     mn = [r for r in recs if r[0] == "mergeN"]
     merge_roofline = {}
@@ -456,7 +470,12 @@ def main():
            "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
            "peak_bf16_tflops": peaks["bf16_tflops"], "peak_source": peak_src,
            "l2": "inputs larger than L2: Q and O are 512 MiB each (K/V 32 MiB each stay L2-resident, as on a CP rank)",
-           "parallelism": f"replicas x{world}"}
+           "parallelism": f"replicas x{world}", "cp_ring_projection": ring}
+    mode_c, kvb, qb = B.choose_mode(q, k, w.n_chunks)
+    cfg["schedule_choice"] = {"model_picks": names[mode_c], "pass_kv_ring_bytes": kvb,
+                              "pass_q_ring_bytes": qb}
+    if len(modes) == 2:
+        cfg["schedule_choice"]["faster_on_one_gpu"] = min(ms_layer, key=ms_layer.get)
 
     # ---- 1M-token layer (ms/layer only)
     if not args.skip_1m and w.name != "1m":

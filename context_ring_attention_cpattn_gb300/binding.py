@@ -51,7 +51,7 @@ EXPORTED = ["cpattn_partial", "cpattn_merge", "cpattn_prefill_workspace_size", "
             "cpattn_prefill_plan", "cpattn_prefill_host_scratch_size", "cpattn_prefill_host",
             "cpattn_prefill_noalloc", "cpattn_decode_workspace_size", "cpattn_decode",
             "cpattn_prefill_ex", "cpattn_prefill_workspace_size_ex", "cpattn_prefill_plan_ex",
-            "cpattn_prefill_critical_path",
+            "cpattn_prefill_critical_path", "cpattn_prefill_choose_mode",
             "cpattn_status_string", "cpattn_device_status",
             "cpattn_profile_begin", "cpattn_profile_end"]
 
@@ -100,6 +100,7 @@ def lib():
     L.cpattn_prefill_plan_ex.argtypes = [i64, i64, i64, i32, i32, i32, O, ctypes.POINTER(PlanEntry),
                                          i32, ctypes.POINTER(ctypes.c_int)]
     L.cpattn_prefill_critical_path.argtypes = [i64, i64, i64, i32, i32, i32, O, dp, dp, dp]
+    L.cpattn_prefill_choose_mode.argtypes = [T, T, i32, ctypes.POINTER(ctypes.c_int), dp, dp]
     L.cpattn_decode.argtypes = [T, T, T, i64, i32, i32, f32, T, vp, vp, ctypes.c_size_t, vp]
     L.cpattn_status_string.argtypes = [i32]
     L.cpattn_status_string.restype = ctypes.c_char_p
@@ -298,6 +299,18 @@ def prefill_plan(sq: int, skv: int, n_chunks: int, mode: int, q_base: int = 0,
         return [(e.step, e.q_chunk, e.kv_chunk, e.role, e.slot, e.launch, e.rank)
                 for e in arr[:n.value]]
     return [(e.step, e.q_chunk, e.kv_chunk, e.role, e.slot) for e in arr[:n.value]]
+
+
+def choose_mode(q, k, n_chunks: int):
+    """(mode, pass_kv_bytes, pass_q_bytes) from the ring traffic model; see
+    cpattn_prefill_choose_mode."""
+    m = ctypes.c_int(0)
+    kvb, qb = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    qv, kv_ = view(q), view(k)
+    _check(lib().cpattn_prefill_choose_mode(ctypes.byref(qv), ctypes.byref(kv_), int(n_chunks),
+                                            ctypes.byref(m), ctypes.byref(kvb), ctypes.byref(qb)),
+           "cpattn_prefill_choose_mode")
+    return m.value, kvb.value, qb.value
 
 
 def critical_path(sq: int, skv: int, n_chunks: int, mode: int, q_base: int = 0,

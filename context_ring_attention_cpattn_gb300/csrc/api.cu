@@ -748,6 +748,22 @@ cpattn_status cpattn_decode(const cpattn_tensor *q, const cpattn_tensor *k, cons
   }
 }
 
+cpattn_status cpattn_prefill_choose_mode(const cpattn_tensor *q, const cpattn_tensor *k,
+                                         int n_chunks, int *mode, double *pass_kv_bytes,
+                                         double *pass_q_bytes) {
+  if (mode == nullptr || q == nullptr || k == nullptr) return CPATTN_ERR_INVALID_ARG;
+  const int es = elem_bytes(q->dtype);
+  if (es == 0 || n_chunks < 1 || q->h < 1 || k->h < 1 || q->d < 1) return CPATTN_ERR_INVALID_ARG;
+  const double N = n_chunks, hops = N * (N - 1);
+  const double ckv = (double)k->s / N, cq = (double)q->s / N;
+  const double kv = hops * 2.0 * ckv * (double)k->h * (double)q->d * es * (double)q->b;
+  const double qb = hops * cq * (double)q->h * ((double)q->d * es * 2.0 + 4.0) * (double)q->b;
+  *mode = qb < kv ? CPATTN_PASS_Q : CPATTN_PASS_KV;
+  if (pass_kv_bytes) *pass_kv_bytes = kv;
+  if (pass_q_bytes) *pass_q_bytes = qb;
+  return CPATTN_OK;
+}
+
 cpattn_status cpattn_prefill_plan(int64_t sq, int64_t skv, int64_t q_base, int n_chunks, int mode,
                                   int causal, cpattn_plan_entry *entries, int capacity,
                                   int *n_entries) {

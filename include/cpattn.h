@@ -240,6 +240,21 @@ cpattn_status cpattn_prefill_critical_path(int64_t sq, int64_t skv, int64_t q_ba
                                            double *step_max, double *critical, double *total);
 
 /*
+ * cpattn_prefill_choose_mode -- pick the ring schedule that moves fewer bytes
+ * between CP ranks (host only; the article's CP section offers both Pass-KV
+ * and Pass-Q without a rule, this is the plainest traffic model).  Over the
+ * N - 1 ring hops every rank forwards one chunk:
+ *   Pass-KV bytes = N (N-1) * 2 * C_kv * hkv * d * es           (K and V travel)
+ *   Pass-Q  bytes = N (N-1) * C_q * hq * (d * es                (Q travels)
+ *                                          + d * es + 4)        (O and LSE return)
+ * with C_kv = skv / N, C_q = sq / N and es the element size.  *mode receives
+ * the cheaper one (ties go to Pass-KV); either byte count pointer may be NULL.
+ */
+cpattn_status cpattn_prefill_choose_mode(const cpattn_tensor *q, const cpattn_tensor *k,
+                                         int n_chunks, int *mode, double *pass_kv_bytes,
+                                         double *pass_q_bytes);
+
+/*
  * cpattn_prefill_host -- end-to-end convenience: q, k, v, o are HOST tensors
  * (pageable or pinned); lse is a host array [b, hq, sq].  Copies inputs to
  * device staging buffers the caller provides (`dev_scratch`, at least

@@ -286,3 +286,22 @@ def test_critical_path_balance(lib):
         assert tot_c / (n * crit_c) < 0.55
         assert tot_z / (n * crit_z) > 0.98
         assert len(steps) == n and abs(sum(steps) - crit_z) < 1e-6
+
+
+def test_choose_mode_traffic_model(lib):
+    """Full prefill with GQA 16:1 moves far fewer bytes as K/V; a decode-shaped
+    query (a few tokens against a long cache) moves fewer bytes as Q."""
+    m, kvb, qb = ctypes.c_int(), ctypes.c_double(), ctypes.c_double()
+    def choose(sq, hq, skv, hkv, n):
+        q, k = T(s=sq, h=hq), T(s=skv, h=hkv)
+        assert lib.cpattn_prefill_choose_mode(ctypes.byref(q), ctypes.byref(k), n, ctypes.byref(m),
+                                              ctypes.byref(kvb), ctypes.byref(qb)) == 0
+        return m.value, kvb.value, qb.value
+    mode, kv, qq = choose(131072, 16, 131072, 1, 16)
+    assert mode == B.PASS_KV and kv == 16 * 15 * 2 * 8192 * 128 * 2
+    assert qq == 16 * 15 * 8192 * 16 * (128 * 2 * 2 + 4)
+    mode, kv, qq = choose(16, 16, 131072, 1, 16)
+    assert mode == B.PASS_Q
+    # The 32K partial prefill: 2 MiB of K/V vs ~2 MiB of Q + returned O per hop.
+    mode, kv, qq = choose(2048, 16, 32768, 1, 8)
+    assert mode == B.PASS_KV and qq > kv
