@@ -220,7 +220,7 @@ def run_reference(args, w):
 
 
 # ----------------------------------------------------------------- GPU arm
-def time_modes(B, w, q, k, v, outs, wss, steps, warmup, world, modes, profile_cap=0):
+def time_modes(B, w, q, k, v, outs, wss, steps, warmup, world, modes, profile_cap=0, launch=0):
     """Warm up, then time `steps` steps, each running the given schedules in
     order.  Returns the elapsed ms (max over ranks), per-schedule ms lists and
     profile records."""
@@ -229,7 +229,7 @@ def time_modes(B, w, q, k, v, outs, wss, steps, warmup, world, modes, profile_ca
     def one(mode):
         o, lse = outs[mode]
         B.prefill(q, k, v, w.n_chunks, mode, q_base=w.q_base, causal=w.causal, out=o, lse=lse,
-                  workspace=wss[mode])
+                  workspace=wss[mode], launch=launch)
 
     for _ in range(warmup):
         for m in modes:
@@ -348,14 +348,14 @@ def time_decode(B, steps, hbm_peak, peak_src, name="decode-128k-b8"):
             "l2": "256 MiB written between calls (L2 flush)", "peak_source": f"{peak_src} HBM copy"}
 
 
-def make_buffers(B, w, q, k, modes):
+def make_buffers(B, w, q, k, modes, launch=0):
     import torch
 
     outs, wss = {}, {}
     for mode in modes:
         outs[mode] = (torch.empty_like(q),
                       torch.empty((w.batch, w.hq, w.sq), dtype=torch.float32, device=q.device))
-        n = B.workspace_size(q, k, w.n_chunks, mode, w.q_base, w.causal)
+        n = B.workspace_size(q, k, w.n_chunks, mode, w.q_base, w.causal, launch=launch)
         wss[mode] = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
     return outs, wss
 
@@ -370,6 +370,8 @@ def main():
     ap.add_argument("--skip-1m", action="store_true", help="do not time the 1M-token layer")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-decode", action="store_true", help="do not time the decode leg")
+    ap.add_argument("--launch", type=int, default=None,
+                    help="ring launch mode: 0 per step, 1 persistent per step, 2 one launch")
     ap.add_argument("--schedules", default="both", choices=["both", "kv", "q"],
                     help="ring schedules in one step (default: Pass-KV then Pass-Q)")
     ap.add_argument("--cpu-rows", type=int, default=2048,
@@ -400,8 +402,9 @@ def main():
 
     modes = {"both": (B.PASS_KV, B.PASS_Q), "kv": (B.PASS_KV,), "q": (B.PASS_Q,)}[args.schedules]
     names = {B.PASS_KV: "pass_kv", B.PASS_Q: "pass_q"}
+    launch = B.LAUNCH_PER_STEP if args.launch is None else args.launch
     q, k, v = make_qkv(w, device="cuda")
-    outs, wss = make_buffers(B, w, q, k, modes)
+    outs, wss = make_buffers(B, w, q, k, modes, launch)
     flops_layer = w.causal_flops()
     flops_step = len(modes) * flops_layer
     launches_per_step = 0
@@ -413,7 +416,7 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     elapsed, per_mode, recs = time_modes(B, w, q, k, v, outs, wss, args.steps, args.warmup, world,
-                                         modes, profile_cap=cap)
+                                         modes, profile_cap=cap, launch=launch)
     clk = clocks.stop()
     ms_step = elapsed / args.steps
     value = world * flops_step * args.steps / (elapsed * 1e-3) / 1e12
@@ -463,6 +466,8 @@ def main():
     decode = None if args.skip_decode else time_decode(B, args.steps, hbm_peak, peak_src)
     cfg = {"workload": w.name, "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim,
            "seq_len": w.sq, "n_chunks": w.n_chunks, "causal": w.causal,
+           "launch_mode": ["one launch per ring step", "persistent CTAs per ring step",
+                           "one persistent launch for all ring steps"][launch],
            "step": " + ".join({"pass_kv": "Pass-KV prefill", "pass_q": "Pass-Q prefill"}[names[m]]
                                for m in modes) + " of one layer",
            "flops_per_layer": flops_layer, "ms_per_layer": ms_layer,
@@ -483,9 +488,10 @@ def main():
         torch.cuda.empty_cache()
         w1 = WORKLOADS["1m"]
         q1, k1, v1 = make_qkv(w1, device="cuda")
-        outs1, wss1 = make_buffers(B, w1, q1, k1, modes)
+        outs1, wss1 = make_buffers(B, w1, q1, k1, modes, launch)
         steps1 = max(1, args.steps // 5)
-        _, pm1, _ = time_modes(B, w1, q1, k1, v1, outs1, wss1, steps1, 1, world, modes)
+        _, pm1, _ = time_modes(B, w1, q1, k1, v1, outs1, wss1, steps1, 1, world, modes,
+                               launch=launch)
         ms1 = {names[m]: statistics.median(pm1[m]) for m in modes}
         f1 = w1.causal_flops()
         cfg["ms_per_layer_1m"] = ms1
@@ -493,7 +499,7 @@ def main():
         cfg["steps_1m"] = steps1
         del outs1, wss1, q1, k1, v1
         torch.cuda.empty_cache()
-        outs, wss = make_buffers(B, w, q, k, modes)
+        outs, wss = make_buffers(B, w, q, k, modes, launch)
 
     # ---- end to end through the host-buffer entry point
     e2e = None

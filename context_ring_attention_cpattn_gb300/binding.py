@@ -33,14 +33,16 @@ class PlanEntry(ctypes.Structure):
 
 
 class PrefillOptions(ctypes.Structure):
-    _fields_ = [("assignment", ctypes.c_int32), ("reserved", ctypes.c_int32 * 7)]
+    _fields_ = [("assignment", ctypes.c_int32), ("launch", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 6)]
 
 
 ASSIGN_CONTIGUOUS, ASSIGN_ZIGZAG = 0, 1
+LAUNCH_PER_STEP, LAUNCH_PERSISTENT_STEP, LAUNCH_SINGLE = 0, 1, 2
 
 
-def _opts(assignment: int):
-    return ctypes.byref(PrefillOptions(int(assignment)))
+def _opts(assignment: int, launch: int = LAUNCH_PER_STEP):
+    return ctypes.byref(PrefillOptions(int(assignment), int(launch)))
 
 
 class ProfileRecord(ctypes.Structure):
@@ -174,19 +176,19 @@ def merge_(o_a, lse_a, o_b, lse_b, stream=None):
 
 
 def workspace_size(q, k, n_chunks: int, mode: int, q_base: int = 0, causal: bool = True,
-                   assignment: int = ASSIGN_CONTIGUOUS) -> int:
+                   assignment: int = ASSIGN_CONTIGUOUS, launch: int = LAUNCH_PER_STEP) -> int:
     n = ctypes.c_size_t(0)
     qv, kv_ = view(q), view(k)
     _check(lib().cpattn_prefill_workspace_size_ex(ctypes.byref(qv), ctypes.byref(kv_), int(q_base),
                                                   int(n_chunks), int(mode), int(bool(causal)),
-                                                  _opts(assignment), ctypes.byref(n)),
+                                                  _opts(assignment, launch), ctypes.byref(n)),
            "cpattn_prefill_workspace_size_ex")
     return n.value
 
 
 def prefill(q, k, v, n_chunks: int, mode: int, q_base: int = 0, causal: bool = True, scale=None,
             out=None, lse=None, workspace=None, out_dtype=None, stream=None,
-            assignment: int = ASSIGN_CONTIGUOUS):
+            assignment: int = ASSIGN_CONTIGUOUS, launch: int = LAUNCH_PER_STEP):
     """CP prefill of one attention layer on one GPU; see cpattn_prefill_ex."""
     import torch
 
@@ -195,7 +197,7 @@ def prefill(q, k, v, n_chunks: int, mode: int, q_base: int = 0, causal: bool = T
         out = torch.empty((B, S, H, D), dtype=out_dtype or q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-    need = workspace_size(q, k, n_chunks, mode, q_base, causal, assignment)
+    need = workspace_size(q, k, n_chunks, mode, q_base, causal, assignment, launch)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
@@ -204,7 +206,8 @@ def prefill(q, k, v, n_chunks: int, mode: int, q_base: int = 0, causal: bool = T
     _check(lib().cpattn_prefill_ex(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
                                    int(q_base), int(n_chunks), int(mode), int(bool(causal)),
                                    float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(), ws_ptr,
-                                   ws_len, _opts(assignment), _stream(stream)), "cpattn_prefill_ex")
+                                   ws_len, _opts(assignment, launch), _stream(stream)),
+           "cpattn_prefill_ex")
     return out, lse
 
 

@@ -299,12 +299,24 @@ struct WsLayout {
   size_t acc_o = 0, acc_lse = 0;      // Pass-KV
   size_t part_o = 0, part_lse = 0;    // Pass-Q
   int64_t slot_o_elems = 0, slot_lse_elems = 0;
+  size_t table = 0, counters = 0;     // one launch for all steps
+  size_t n_counters = 0;
   size_t total = 0;
 };
 
-WsLayout ws_layout(const Plan &pl, int64_t B, int64_t sq, int64_t hq, int64_t d) {
+int64_t tiles_per_piece(const Plan &pl) { return (pl.Cq + 127) / 128; }
+
+WsLayout ws_layout(const Plan &pl, int64_t B, int64_t sq, int64_t hq, int64_t d,
+                   int launch_mode = CPATTN_LAUNCH_PER_STEP) {
   WsLayout w;
   size_t off = 0;
+  if (launch_mode == CPATTN_LAUNCH_SINGLE) {
+    w.table = off;
+    off = align256(off + pl.entries.size() * sizeof(PairDesc));
+    w.counters = off;
+    w.n_counters = (size_t)pl.P * tiles_per_piece(pl) * hq * B;
+    off = align256(off + w.n_counters * sizeof(int32_t));
+  }
   if (pl.mode == CPATTN_PASS_KV && pl.need_acc) {
     w.acc_o = off;
     off = align256(off + (size_t)B * sq * hq * d * 4);
@@ -323,12 +335,14 @@ WsLayout ws_layout(const Plan &pl, int64_t B, int64_t sq, int64_t hq, int64_t d)
   return w;
 }
 
-cudaError_t launch_attn(AttnParams &p, cudaStream_t st, const cpattn_tensor *q) {
+cudaError_t launch_attn(AttnParams &p, cudaStream_t st, const cpattn_tensor *q,
+                        double vis_override = -1.0) {
   double vis = 0.0;
   for (int x = 0; x < p.n_pairs; ++x) {
     const PairDesc &pd = p.pairs[x];
     vis += visible_pairs(pd.delta, pd.q_len, 0, pd.kv_len, p.causal != 0);
   }
+  if (vis_override >= 0.0) vis = vis_override;
   const double flops = 4.0 * (double)q->d * (double)q->h * (double)q->b * vis;
   const bool tc = attn_tc_supported(p);
   prof_before(st);
@@ -339,6 +353,10 @@ cudaError_t launch_attn(AttnParams &p, cudaStream_t st, const cpattn_tensor *q) 
 
 int assignment_of(const cpattn_prefill_options *opts) {
   return opts ? opts->assignment : CPATTN_ASSIGN_CONTIGUOUS;
+}
+
+int launch_mode_of(const cpattn_prefill_options *opts) {
+  return opts ? opts->launch : CPATTN_LAUNCH_DEFAULT;
 }
 
 cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const cpattn_tensor *v,
@@ -352,7 +370,11 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
   if ((s = build_plan(q->s, k->s, q_base, n_chunks, mode, causal, assignment_of(opts), pl)) !=
       CPATTN_OK)
     return s;
-  const WsLayout wl = ws_layout(pl, q->b, q->s, q->h, q->d);
+  const int lmode = launch_mode_of(opts);
+  if (lmode != CPATTN_LAUNCH_PER_STEP && lmode != CPATTN_LAUNCH_PERSISTENT_STEP &&
+      lmode != CPATTN_LAUNCH_SINGLE)
+    return CPATTN_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(pl, q->b, q->s, q->h, q->d, lmode);
   if (wl.total > 0) {
     if (workspace == nullptr || ws_bytes < wl.total) return CPATTN_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return CPATTN_ERR_WORKSPACE;
@@ -386,13 +408,8 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
     p.part_lse_stride = wl.slot_lse_elems;
   }
 
-  // One launch per ring step (two per step for zigzag Pass-KV, one per
-  // visiting K/V piece); pairs ordered by work, largest first.
-  size_t e0 = 0;
-  for (int l = 0; l < pl.n_launches; ++l) {
-    size_t e1 = e0;
-    while (e1 < pl.entries.size() && pl.entries[e1].launch == l) ++e1;
-    if (e1 == e0) continue;
+  // Pairs of each launch ordered by work, largest first.
+  auto launch_items = [&](size_t e0, size_t e1, std::vector<PairDesc> &out) {
     struct Item { PairDesc pd; double work; };
     std::vector<Item> items;
     for (size_t x = e0; x < e1; ++x) {
@@ -406,13 +423,74 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
       it.pd.delta = q_base + (int64_t)e.q_chunk * pl.Cq - (int64_t)e.kv_chunk * pl.C;
       it.pd.mode = e.role;
       it.pd.slot = e.slot;
+      it.pd.dep_base = (int32_t)((int64_t)e.q_chunk * tiles_per_piece(pl) * q->h * q->b);
       it.work = visible_pairs(it.pd.delta, pl.Cq, 0, pl.C, causal != 0);
       items.push_back(it);
     }
     std::stable_sort(items.begin(), items.end(),
                      [](const Item &a, const Item &b) { return a.work > b.work; });
+    for (const auto &it : items) out.push_back(it.pd);
+  };
+
+  if (lmode == CPATTN_LAUNCH_SINGLE && attn_tc_supported(p)) {
+    // One persistent launch for every ring step.  Work items keep the ring's
+    // launch order; a Pass-KV accumulator update waits (bounded) until the
+    // previous visit of the same rows has finished.
+    std::vector<PairDesc> table;
+    size_t e0 = 0;
+    for (int l = 0; l < pl.n_launches; ++l) {
+      size_t e1 = e0;
+      while (e1 < pl.entries.size() && pl.entries[e1].launch == l) ++e1;
+      launch_items(e0, e1, table);
+      e0 = e1;
+    }
+    const int nt = attn_tc_tiles_per_cta(p);
+    std::vector<int> visits(pl.P, 0);
+    int total = 0;
+    double vis = 0.0;
+    for (auto &pd : table) {
+      pd.n_qtiles = (pd.q_len + 127) / 128;
+      pd.cta_begin = total;
+      total += pd.n_qtiles * (int)(q->h / nt) * (int)q->b;
+      const int piece = (int)(pd.q_row0 / pl.Cq);
+      if (pd.mode == kAccInit || pd.mode == kAccMerge || pd.mode == kAccFinal)
+        pd.visit = visits[piece]++;
+      vis += visible_pairs(pd.delta, pd.q_len, 0, pd.kv_len, causal != 0);
+    }
+    if (total > 0) {
+      PairDesc *dev_table = reinterpret_cast<PairDesc *>(ws + wl.table);
+      if (cudaMemcpyAsync(dev_table, table.data(), table.size() * sizeof(PairDesc),
+                          cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return CPATTN_ERR_CUDA;
+      p.pair_table = dev_table;
+      p.n_table = (int32_t)table.size();
+      p.total_ctas = total;
+      p.persistent_ctas = 1;
+      if (pl.mode == CPATTN_PASS_KV && pl.need_acc) {
+        p.dep_counters = reinterpret_cast<int32_t *>(ws + wl.counters);
+        if (cudaMemsetAsync(p.dep_counters, 0, wl.n_counters * sizeof(int32_t), st) != cudaSuccess)
+          return CPATTN_ERR_CUDA;
+      }
+      if (launch_attn(p, st, q, vis) != cudaSuccess) return CPATTN_ERR_CUDA;
+      p.pair_table = nullptr;
+      p.n_table = 0;
+      p.dep_counters = nullptr;
+      p.persistent_ctas = 0;
+    }
+  }
+  // One launch per ring step (two per step for zigzag Pass-KV, one per
+  // visiting K/V piece).
+  const bool per_step = !(lmode == CPATTN_LAUNCH_SINGLE && attn_tc_supported(p));
+  p.persistent_ctas = lmode == CPATTN_LAUNCH_PERSISTENT_STEP ? 1 : 0;
+  size_t e0 = 0;
+  for (int l = 0; l < pl.n_launches && per_step; ++l) {
+    size_t e1 = e0;
+    while (e1 < pl.entries.size() && pl.entries[e1].launch == l) ++e1;
+    if (e1 == e0) continue;
+    std::vector<PairDesc> items;
+    launch_items(e0, e1, items);
     p.n_pairs = (int32_t)items.size();
-    for (size_t x = 0; x < items.size(); ++x) p.pairs[x] = items[x].pd;
+    for (size_t x = 0; x < items.size(); ++x) p.pairs[x] = items[x];
     if (launch_attn(p, st, q) != cudaSuccess) return CPATTN_ERR_CUDA;
     e0 = e1;
   }
@@ -627,7 +705,7 @@ cpattn_status cpattn_prefill_workspace_size_ex(const cpattn_tensor *q, const cpa
     if ((s = build_plan(q->s, k->s, q_base, n_chunks, mode, causal, assignment_of(opts), pl)) !=
         CPATTN_OK)
       return s;
-    *bytes = ws_layout(pl, q->b, q->s, q->h, q->d).total;
+    *bytes = ws_layout(pl, q->b, q->s, q->h, q->d, launch_mode_of(opts)).total;
     return CPATTN_OK;
   } catch (...) {
     return CPATTN_ERR_INVALID_ARG;
@@ -720,6 +798,7 @@ cpattn_status cpattn_decode(const cpattn_tensor *q, const cpattn_tensor *k, cons
       if (dp.packed) {
         p.pack_g = (int32_t)(q->h / k->h);
         p.kv_split = dp.kv_split;
+        p.persistent_ctas = 1;  // many short items: loop over them, one CTA per SM
       }
       if (launch_attn(p, st, q) != cudaSuccess) return CPATTN_ERR_CUDA;
     }

@@ -66,14 +66,16 @@ struct Layout {
   static constexpr int bar_off = v_off + kStages * kTileBytes;
   // barrier indices
   static constexpr int b_qfull = 0;
-  static constexpr int b_kfull = 1;
+  static constexpr int b_qempty = 1;  // the item's last QK MMA is done with Q
+  static constexpr int b_kfull = 2;
   static constexpr int b_kempty = b_kfull + kStages;
   static constexpr int b_vfull = b_kempty + kStages;
   static constexpr int b_vempty = b_vfull + kStages;
   static constexpr int b_sfull = b_vempty + kStages;
   static constexpr int b_pready = b_sfull + NT;
   static constexpr int b_pvdone = b_pready + NT;
-  static constexpr int b_drain = b_pvdone + NT;
+  static constexpr int b_ofree = b_pvdone + NT;  // softmax warps have read O_t
+  static constexpr int b_drain = b_ofree + NT;
   static constexpr int n_bars = b_drain + 1;
   static constexpr int tmem_slot_off = bar_off + n_bars * 8;
   static constexpr int abort_off = tmem_slot_off + 4;
@@ -233,7 +235,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // ---------------------------------------------------------------- kernel
-template <int NT, bool kStrictOrder>
+// Kernel parameters (three tensor maps and the parameter block) must fit the
+// 4 KB kernel-parameter space.
+static_assert(sizeof(AttnParams) + 3 * sizeof(CUtensorMap) <= 4096, "kernel parameters too large");
+
+template <int NT, bool kStrictOrder, bool kPersistent>
 __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnParams p) {
@@ -246,55 +252,19 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::abort_off);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // ---- work item
-  //   per-head tiles (pack_g == 0): (pair, query tile, head group, batch)
-  //   packed decode tiles (pack_g > 0, NT == 1): (pair, kv split, kv head, batch)
-  int pi = 0;
-  while (pi + 1 < p.n_pairs && (int)blockIdx.x >= p.pairs[pi + 1].cta_begin) ++pi;
-  const PairDesc &pd = p.pairs[pi];
-  int local = (int)blockIdx.x - pd.cta_begin;
+  const PairDesc *pairs = p.pair_table != nullptr ? p.pair_table : p.pairs;
+  const int n_pairs = p.pair_table != nullptr ? p.n_table : p.n_pairs;
   const int G = NT == 1 ? p.pack_g : 0;  // query heads per tile in packed mode, else 0
-  int h0, hk, i0, q_rows, split = 0;
-  int64_t ks = 0, ke = pd.kv_len;  // this CTA's keys [ks, ke) of the pair
-  if (G == 0) {
-    const int n_hg = p.Hq / NT;
-    const int hg = local % n_hg;
-    local /= n_hg;
-    const int qt = pd.n_qtiles - 1 - local / p.B;  // longest tiles first
-    h0 = hg * NT;
-    hk = h0 / (p.Hq / p.Hkv);
-    i0 = qt * kBM;
-    q_rows = min(kBM, pd.q_len - i0);
-  } else {
-    hk = local % p.Hkv;
-    local /= p.Hkv;
-    split = local / p.B;
-    h0 = hk * G;
-    i0 = 0;
-    q_rows = pd.q_len;
-    ks = (int64_t)split * p.kv_split;
-    ke = ks + p.kv_split < ke ? ks + p.kv_split : ke;
-  }
-  const int b = local % p.B;
+  // Work items handled by this CTA: blockIdx.x, + stride, ... (one item when
+  // the grid has a CTA per item; a loop in a persistent launch).
+  // A non-persistent launch runs exactly one item per CTA, which the compiler
+  // sees (kPersistent false), so no state is carried between items.
+  const int stride = kPersistent ? (int)gridDim.x : p.total_ctas;
 
-  // Keys [ks, kv_end) are visible to some row of the tile; keys [ks, full_end)
-  // to every row.
-  int64_t kv_end = ke, full_end = ke;
-  if (p.causal) {
-    const int64_t last_lim = (int64_t)(i0 + q_rows - 1) + pd.delta + 1;
-    const int64_t first_lim = (int64_t)i0 + pd.delta + 1;
-    kv_end = last_lim < kv_end ? last_lim : kv_end;
-    full_end = first_lim < full_end ? first_lim : full_end;
-  }
-  if (kv_end < ks) kv_end = ks;
-  if (full_end < ks) full_end = ks;
-  const int n_kv = (int)((kv_end - ks + kBN - 1) / kBN);
-  const int n_unmasked = (int)((full_end - ks) / kBN);
-
-  // ---- setup
+  // ---- setup (once per CTA)
   if (threadIdx.x == 0) {
     mbar_init(bar(L::b_qfull), 1);
+    mbar_init(bar(L::b_qempty), 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::b_kfull + s), 1);
       mbar_init(bar(L::b_kempty + s), 1);
@@ -305,6 +275,7 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
       mbar_init(bar(L::b_sfull + t), 1);
       mbar_init(bar(L::b_pready + t), 4);
       mbar_init(bar(L::b_pvdone + t), 1);
+      mbar_init(bar(L::b_ofree + t), 4);
     }
     mbar_init(bar(L::b_drain), 1);
     *abort_flag = 0;
@@ -325,42 +296,110 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::tmem_slot_off);
 
+  // ---- work item geometry (every role decodes the same items identically)
+  //   per-head tiles (pack_g == 0): (pair, query tile, head group, batch)
+  //   packed decode tiles (pack_g > 0, NT == 1): (pair, kv split, kv head, batch)
+  struct Item {
+    const PairDesc *pd;
+    int h0, hk, i0, q_rows, split, b, qt, n_kv, n_unmasked;
+    int64_t ks, ke;  // this item's keys [ks, ke) of the pair
+  };
+  auto decode = [&](int item, Item &it) {
+    int lo = 0, hi = n_pairs - 1;  // last pair whose cta_begin <= item
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pairs[mid].cta_begin <= item) lo = mid; else hi = mid - 1;
+    }
+    const PairDesc &pd = pairs[lo];
+    it.pd = &pd;
+    int local = item - pd.cta_begin;
+    it.split = 0;
+    it.ks = 0;
+    it.ke = pd.kv_len;
+    if (G == 0) {
+      const int n_hg = p.Hq / NT;
+      const int hg = local % n_hg;
+      local /= n_hg;
+      it.qt = pd.n_qtiles - 1 - local / p.B;  // longest tiles first
+      it.h0 = hg * NT;
+      it.hk = it.h0 / (p.Hq / p.Hkv);
+      it.i0 = it.qt * kBM;
+      it.q_rows = min(kBM, pd.q_len - it.i0);
+    } else {
+      it.hk = local % p.Hkv;
+      local /= p.Hkv;
+      it.split = local / p.B;
+      it.qt = 0;
+      it.h0 = it.hk * G;
+      it.i0 = 0;
+      it.q_rows = pd.q_len;
+      it.ks = (int64_t)it.split * p.kv_split;
+      it.ke = it.ks + p.kv_split < it.ke ? it.ks + p.kv_split : it.ke;
+    }
+    it.b = local % p.B;
+    // Keys [ks, kv_end) are visible to some row of the tile; [ks, full_end) to every row.
+    int64_t kv_end = it.ke, full_end = it.ke;
+    if (p.causal) {
+      const int64_t last_lim = (int64_t)(it.i0 + it.q_rows - 1) + pd.delta + 1;
+      const int64_t first_lim = (int64_t)it.i0 + pd.delta + 1;
+      kv_end = last_lim < kv_end ? last_lim : kv_end;
+      full_end = first_lim < full_end ? first_lim : full_end;
+    }
+    if (kv_end < it.ks) kv_end = it.ks;
+    if (full_end < it.ks) full_end = it.ks;
+    it.n_kv = (int)((kv_end - it.ks + kBN - 1) / kBN);
+    it.n_unmasked = (int)((full_end - it.ks) / kBN);
+  };
+
   if (warp == L::kTmaWarp) {
     // ================================================= TMA producer
-    if (lane == 0 && n_kv > 0) {
-      int issued_k[L::kStages] = {0}, issued_v[L::kStages] = {0};
-      bool q_issued = false, ok = true;
-      mbar_expect_tx(bar(L::b_qfull), NT * kTileBytes);
-      for (int t = 0; t < NT; ++t)
-        for (int half = 0; half < 2; ++half)
-          tma_load_4d(sb + L::q_off + t * kTileBytes + half * kBoxBytes, &tm_q, bar(L::b_qfull),
-                      half * 64, h0 + t, pd.q_row0 + i0, b);  // packed map: heads h0.., rows 0..
-      q_issued = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int st = j % L::kStages;
-        const int kv_row = pd.kv_row0 + (int)ks + j * kBN;
-        if (j >= L::kStages && !wait_bar(bar(L::b_kempty + st), ((j / L::kStages) - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
+    // K/V loads count up across items (stage g % S, phase g / S); Q of an
+    // item waits until the previous item's QK MMAs are done with Q.
+    if (lane == 0) {
+      int issued_k[L::kStages] = {0}, issued_v[L::kStages] = {0}, issued_q = 0;
+      int g = 0, nitem = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < p.total_ctas && ok; item += stride) {
+        Item it;
+        decode(item, it);
+        if (it.n_kv == 0) continue;
+        if (nitem > 0 && !wait_bar(bar(L::b_qempty), (nitem - 1) & 1, abort_flag)) { ok = false; break; }
+        mbar_expect_tx(bar(L::b_qfull), NT * kTileBytes);
+        for (int t = 0; t < NT; ++t)
+          for (int half = 0; half < 2; ++half)
+            tma_load_4d(sb + L::q_off + t * kTileBytes + half * kBoxBytes, &tm_q, bar(L::b_qfull),
+                        half * 64, it.h0 + t, it.pd->q_row0 + it.i0, it.b);  // packed map: heads h0..
+        ++issued_q;
+        for (int j = 0; j < it.n_kv; ++j, ++g) {
+          const int st = g % L::kStages;
+          const int kv_row = it.pd->kv_row0 + (int)it.ks + j * kBN;
+          if (g >= L::kStages &&
+              !wait_bar(bar(L::b_kempty + st), ((g / L::kStages) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bar(L::b_kfull + st), kTileBytes);
+          for (int half = 0; half < 2; ++half)
+            tma_load_4d(sb + L::k_off + st * kTileBytes + half * kBoxBytes, &tm_k,
+                        bar(L::b_kfull + st), half * 64, it.hk, kv_row, it.b);
+          ++issued_k[st];
+          if (g >= L::kStages &&
+              !wait_bar(bar(L::b_vempty + st), ((g / L::kStages) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bar(L::b_vfull + st), kTileBytes);
+          for (int half = 0; half < 2; ++half)
+            tma_load_4d(sb + L::v_off + st * kTileBytes + half * kBoxBytes, &tm_v,
+                        bar(L::b_vfull + st), half * 64, it.hk, kv_row, it.b);
+          ++issued_v[st];
         }
-        mbar_expect_tx(bar(L::b_kfull + st), kTileBytes);
-        for (int half = 0; half < 2; ++half)
-          tma_load_4d(sb + L::k_off + st * kTileBytes + half * kBoxBytes, &tm_k,
-                      bar(L::b_kfull + st), half * 64, hk, kv_row, b);
-        ++issued_k[st];
-        if (j >= L::kStages && !wait_bar(bar(L::b_vempty + st), ((j / L::kStages) - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        mbar_expect_tx(bar(L::b_vfull + st), kTileBytes);
-        for (int half = 0; half < 2; ++half)
-          tma_load_4d(sb + L::v_off + st * kTileBytes + half * kBoxBytes, &tm_v,
-                      bar(L::b_vfull + st), half * 64, hk, kv_row, b);
-        ++issued_v[st];
+        ++nitem;
+        if constexpr (!kPersistent) break;
       }
       if (!ok) {
         // Let the copies already in flight land before the CTA exits.
-        if (q_issued) wait_bar(bar(L::b_qfull), 0, abort_flag, false);
+        if (issued_q > 0) wait_bar(bar(L::b_qfull), (issued_q - 1) & 1, abort_flag, false);
         for (int s = 0; s < L::kStages; ++s) {
           if (issued_k[s] > 0) wait_bar(bar(L::b_kfull + s), (issued_k[s] - 1) & 1, abort_flag, false);
           if (issued_v[s] > 0) wait_bar(bar(L::b_vfull + s), (issued_v[s] - 1) & 1, abort_flag, false);
@@ -379,8 +418,9 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
     // pipe executing one thread's MMAs in issue order (PTX states that order
     // only for MMAs sharing an accumulator); kStrictOrder inserts a wait for
     // the PV MMA to complete before S_t(j+1) is issued.
-    if (lane == 0 && n_kv > 0) {
-      bool ok = wait_bar(bar(L::b_qfull), 0, abort_flag);
+    // Across items: the first PV of an item (which overwrites O_t) waits until
+    // the softmax warps have read the previous item's O_t (ofree_t).
+    if (lane == 0) {
       // Descriptors of the first 16-column slice of tile 0 / stage 0 of each
       // operand; other tiles, stages and slices add their byte offset (>> 4)
       // to the start-address field (shared memory stays below 256 KB, so the
@@ -406,44 +446,71 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
                  dv + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
         }
       };
-      if (ok) ok = wait_bar(bar(L::b_kfull + 0), 0, abort_flag);
-      if (ok) {
+      bool ok = true;
+      int g = 0, nitem = 0;  // KV steps and non-empty items issued so far
+      for (int item = blockIdx.x; item < p.total_ctas && ok; item += stride) {
+        Item it;
+        decode(item, it);
+        const int n_kv = it.n_kv;
+        if (n_kv == 0) continue;
+        if (!wait_bar(bar(L::b_qfull), nitem & 1, abort_flag) ||
+            !wait_bar(bar(L::b_kfull + g % L::kStages), (g / L::kStages) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (kStrictOrder && nitem > 0) {
+          // S_t(0) overwrites P_t of the previous item's last PV.
+          for (int t = 0; t < NT && ok; ++t)
+            ok = wait_bar(bar(L::b_pvdone + t), (g - 1) & 1, abort_flag);
+          if (!ok) break;
+        }
         tc_fence_after();
         for (int t = 0; t < NT; ++t) {
-          issue_qk(t, 0);
+          issue_qk(t, g % L::kStages);
           mma_commit(bar(L::b_sfull + t));
         }
-        mma_commit(bar(L::b_kempty + 0));
-      }
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int st = j % L::kStages;
-        const int st1 = (j + 1) % L::kStages;
-        const bool more = j + 1 < n_kv;
-        for (int t = 0; t < NT && ok; ++t) {
-          // Each wait sits right before the first MMA that needs it.
-          if ((t == 0 && !wait_bar(bar(L::b_vfull + st), (j / L::kStages) & 1, abort_flag)) ||
-              !wait_bar(bar(L::b_pready + t), j & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_pv(t, st, j > 0);
-          if (t == NT - 1) mma_commit(bar(L::b_vempty + st));
-          if (kStrictOrder || !more) mma_commit(bar(L::b_pvdone + t));
-          if (more) {
-            if (t == 0 && !wait_bar(bar(L::b_kfull + st1), ((j + 1) / L::kStages) & 1, abort_flag)) {
+        mma_commit(bar(L::b_kempty + g % L::kStages));
+        if (kPersistent && n_kv == 1) mma_commit(bar(L::b_qempty));
+        for (int j = 0; j < n_kv && ok; ++j) {
+          const int gj = g + j;
+          const int st = gj % L::kStages;
+          const int st1 = (gj + 1) % L::kStages;
+          const bool more = j + 1 < n_kv;
+          for (int t = 0; t < NT && ok; ++t) {
+            // Each wait sits right before the first MMA that needs it.
+            if ((t == 0 && !wait_bar(bar(L::b_vfull + st), (gj / L::kStages) & 1, abort_flag)) ||
+                !wait_bar(bar(L::b_pready + t), gj & 1, abort_flag) ||
+                (kPersistent && j == 0 && nitem > 0 &&
+                 !wait_bar(bar(L::b_ofree + t), (nitem - 1) & 1, abort_flag))) {
               ok = false;
               break;
             }
-            if (kStrictOrder) {
-              if (!wait_bar(bar(L::b_pvdone + t), j & 1, abort_flag)) { ok = false; break; }
-            }
             tc_fence_after();
-            issue_qk(t, st1);
-            mma_commit(bar(L::b_sfull + t));
-            if (t == NT - 1) mma_commit(bar(L::b_kempty + st1));
+            issue_pv(t, st, j > 0);
+            if (t == NT - 1) mma_commit(bar(L::b_vempty + st));
+            if (kStrictOrder || !more) mma_commit(bar(L::b_pvdone + t));
+            if (more) {
+              if (t == 0 &&
+                  !wait_bar(bar(L::b_kfull + st1), ((gj + 1) / L::kStages) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              if (kStrictOrder) {
+                if (!wait_bar(bar(L::b_pvdone + t), gj & 1, abort_flag)) { ok = false; break; }
+              }
+              tc_fence_after();
+              issue_qk(t, st1);
+              mma_commit(bar(L::b_sfull + t));
+              if (t == NT - 1) {
+                mma_commit(bar(L::b_kempty + st1));
+                if (kPersistent && j + 2 == n_kv) mma_commit(bar(L::b_qempty));  // last QK
+              }
+            }
           }
         }
+        g += n_kv;
+        ++nitem;
+        if constexpr (!kPersistent) break;
       }
       if (!ok) {
         mma_commit(bar(L::b_drain));
@@ -459,107 +526,142 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t t_s = tmem + lane_off + t * 128;
     const uint32_t t_o = tmem + lane_off + (NT + t) * 128;
-    // Query row (inside the pair's chunk) and head of this tile row.
-    const int qrow = G == 0 ? i0 + r : r / G;
-    const int head = G == 0 ? h0 + t : h0 + r % G;
-    const bool valid = G == 0 ? r < q_rows : qrow < q_rows;
-    int64_t lim = ke;  // this row's visible keys: [ks, lim)
-    if (p.causal) {
-      const int64_t c = (int64_t)qrow + pd.delta + 1;
-      lim = c < lim ? c : lim;
-    }
     const float sl2 = p.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      // Warp-uniform outcome: the TMEM accesses below are warp-collective.
-      if (!__all_sync(0xffffffffu, wait_bar(bar(L::b_sfull + t), j & 1, abort_flag))) {
-        ok = false;
-        break;
+    int g = 0, nitem = 0;
+    for (int item = blockIdx.x; item < p.total_ctas && ok; item += stride) {
+      Item it;
+      decode(item, it);
+      const PairDesc &pd = *it.pd;
+      const int n_kv = it.n_kv;
+      // Query row (inside the pair's chunk) and head of this tile row.
+      const int qrow = G == 0 ? it.i0 + r : r / G;
+      const int head = G == 0 ? it.h0 + t : it.h0 + r % G;
+      const bool valid = G == 0 ? r < it.q_rows : qrow < it.q_rows;
+      int64_t lim = it.ke;  // this row's visible keys: [ks, lim)
+      if (p.causal) {
+        const int64_t c = (int64_t)qrow + pd.delta + 1;
+        lim = c < lim ? c : lim;
       }
-      tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld_x128(t_s, sr);
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < kBN; ++c) s[c] = __uint_as_float(sr[c]);
-      if (j >= n_unmasked) {
-        int64_t nv = lim - ks - (int64_t)j * kBN;
-        const int nvis = nv < 0 ? 0 : (nv > kBN ? kBN : (int)nv);
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c >= nvis) s[c] = -INFINITY;
-      }
-      // Row max: eight independent chains of 3-input maxima (short
-      // dependency chains keep the softmax off the MMA critical path).
-      float mk[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float m = fmax3(s[k], s[k + 8], s[k + 16]);
-#pragma unroll
-        for (int i = 3; i < 15; i += 2) m = fmax3(m, s[k + 8 * i], s[k + 8 * (i + 1)]);
-        mk[k] = fmaxf(m, s[k + 120]);
-      }
-      const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
-                             fmaxf(mk[6], mk[7]));
-      const float m_new = fmaxf(m_run, mx * sl2);
-      const bool grow = m_new > m_run + kRescaleLog2;
-      float alpha = 1.f;
-      if (grow) {
-        alpha = ex2(m_run - m_new);  // 0 when m_run = -inf
-        l_run *= alpha;
-      }
-      const bool rescale_o = grow && (m_run != -INFINITY) && j > 0;
-      if (grow) m_run = m_new;
-      if (__any_sync(0xffffffffu, rescale_o)) {
-        const float a = rescale_o ? alpha : 1.f;
-#pragma unroll
-        for (int cc = 0; cc < kD / 32; ++cc) {
-          uint32_t ov[32];
-          tmem_ld_x32(t_o + cc * 32, ov);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * a);
-          tmem_st_x32(t_o + cc * 32, ov);
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < n_kv; ++j) {
+        // Warp-uniform outcome: the TMEM accesses below are warp-collective.
+        if (!__all_sync(0xffffffffu, wait_bar(bar(L::b_sfull + t), (g + j) & 1, abort_flag))) {
+          ok = false;
+          break;
         }
-      }
-      // p = 2^(s * scale * log2e - m): the scale-and-shift runs two columns per
-      // instruction (f32x2 FMA), the row sum in four independent f32x2 chains.
-      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-      const float2 sl2v = make_float2(sl2, sl2);
-      const float2 negm = make_float2(neg_m, neg_m);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
-      uint32_t pk[64];
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld_x128(t_s, sr);
+        float s[128];
 #pragma unroll
-      for (int c = 0; c < kBN; c += 2) {
-        const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2v, negm);
-        const float2 pv = make_float2(ex2(x.x), ex2(x.y));
-        acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], pv);
-        pk[c >> 1] = pack_bf16(pv.x, pv.y);
+        for (int c = 0; c < kBN; ++c) s[c] = __uint_as_float(sr[c]);
+        if (j >= it.n_unmasked) {
+          int64_t nv = lim - it.ks - (int64_t)j * kBN;
+          const int nvis = nv < 0 ? 0 : (nv > kBN ? kBN : (int)nv);
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c >= nvis) s[c] = -INFINITY;
+        }
+        // Row max: eight independent chains of 3-input maxima (short
+        // dependency chains keep the softmax off the MMA critical path).
+        float mk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          float m = fmax3(s[k], s[k + 8], s[k + 16]);
+#pragma unroll
+          for (int i = 3; i < 15; i += 2) m = fmax3(m, s[k + 8 * i], s[k + 8 * (i + 1)]);
+          mk[k] = fmaxf(m, s[k + 120]);
+        }
+        const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
+                               fmaxf(mk[6], mk[7]));
+        const float m_new = fmaxf(m_run, mx * sl2);
+        const bool grow = m_new > m_run + kRescaleLog2;
+        float alpha = 1.f;
+        if (grow) {
+          alpha = ex2(m_run - m_new);  // 0 when m_run = -inf
+          l_run *= alpha;
+        }
+        const bool rescale_o = grow && (m_run != -INFINITY) && j > 0;
+        if (grow) m_run = m_new;
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          const float a = rescale_o ? alpha : 1.f;
+#pragma unroll
+          for (int cc = 0; cc < kD / 32; ++cc) {
+            uint32_t ov[32];
+            tmem_ld_x32(t_o + cc * 32, ov);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * a);
+            tmem_st_x32(t_o + cc * 32, ov);
+          }
+        }
+        // p = 2^(s * scale * log2e - m): the scale-and-shift runs two columns per
+        // instruction (f32x2 FMA), the row sum in four independent f32x2 chains.
+        const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+        const float2 sl2v = make_float2(sl2, sl2);
+        const float2 negm = make_float2(neg_m, neg_m);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+        // Four quarters of 32 columns: each quarter's P is stored (16 packed
+        // columns) as soon as it exists, so few registers stay live.
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = qq * 32; c < qq * 32 + 32; c += 2) {
+            const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2v, negm);
+            const float2 pv = make_float2(ex2(x.x), ex2(x.y));
+            acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], pv);
+            pk[(c >> 1) - qq * 16] = pack_bf16(pv.x, pv.y);
+          }
+          tmem_st_x16(t_s + qq * 16, pk);
+        }
+        const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+        const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+        const float2 a03 = __fadd2_rn(a01, a23);
+        l_run += a03.x + a03.y;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::b_pready + t));
       }
-      const float2 a01 = __fadd2_rn(acc[0], acc[1]);
-      const float2 a23 = __fadd2_rn(acc[2], acc[3]);
-      const float2 a03 = __fadd2_rn(a01, a23);
-      l_run += a03.x + a03.y;
-      tmem_st_x64(t_s, pk);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::b_pready + t));
-    }
+      if (!ok) break;
 
-    // ---- epilogue: O_t / l, LSE, routed by the pair's role
-    if (ok && n_kv > 0) {
-      // pvdone_t completes once per KV step in the strict schedule, else once.
-      const uint32_t par = kStrictOrder ? ((n_kv - 1) & 1) : 0u;
-      ok = __all_sync(0xffffffffu, wait_bar(bar(L::b_pvdone + t), par, abort_flag));
-      tc_fence_after();
-    }
-    if (__all_sync(0xffffffffu, ok && !*abort_flag)) {
+      // ---- epilogue: O_t / l, LSE, routed by the pair's role
+      if (n_kv > 0) {
+        // pvdone_t completes once per KV step in the strict schedule, else once per item.
+        const uint32_t par = kStrictOrder ? ((g + n_kv - 1) & 1) : (nitem & 1);
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::b_pvdone + t), par, abort_flag));
+        tc_fence_after();
+        if (!ok) break;
+      }
+      // One launch for all Pass-KV steps: accumulator updates of a tile row
+      // block happen in visit order (progress counter per tile, head, batch).
+      int32_t *dep = nullptr;
+      if (kPersistent && p.dep_counters != nullptr && G == 0 &&
+          (pd.mode == kAccInit || pd.mode == kAccMerge || pd.mode == kAccFinal))
+        dep = p.dep_counters + pd.dep_base + ((int64_t)it.qt * p.Hq + head) * p.B + it.b;
+      if (dep != nullptr && pd.visit > 0) {
+        if (warp % 4 == 0 && lane == 0) {
+          const unsigned long long t0 = global_ns();
+          for (uint32_t spin = 0;; ++spin) {
+            int v;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(dep) : "memory");
+            if (v >= pd.visit) break;
+            if ((spin & 63u) == 63u && (*abort_flag || global_ns() - t0 > kWaitNs)) {
+              *abort_flag = 1;
+              atomicOr(&g_attn_tc_status, 1u);
+              break;
+            }
+          }
+        }
+        asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");
+        if (*abort_flag) { ok = false; break; }
+      }
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       RowSink sink;
-      if (valid) sink.init(p, pd, b, head, qrow, lse, true, G == 0 ? -1 : pd.slot + split);
+      if (valid) sink.init(p, pd, it.b, head, qrow, lse, true, G == 0 ? -1 : pd.slot + it.split);
 #pragma unroll 1
       for (int cc = 0; cc < kD / 32; ++cc) {
         float ov[32];
@@ -574,6 +676,22 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
         }
         if (valid) sink.put<32>(cc * 32, ov);
       }
+      if (kPersistent && n_kv > 0) {
+        // O_t has been read: the next item's first PV may overwrite it.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::b_ofree + t));
+      }
+      if (dep != nullptr && pd.mode != kAccFinal) {
+        asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");
+        if (warp % 4 == 0 && lane == 0) {
+          __threadfence();
+          asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(dep), "r"(pd.visit + 1) : "memory");
+        }
+      }
+      g += n_kv;
+      if (n_kv > 0) ++nitem;
+      if constexpr (!kPersistent) break;
     }
   }
 
@@ -621,11 +739,15 @@ bool make_map(CUtensorMap *map, const void *base, int64_t B, int64_t S, int64_t 
   return r == CUDA_SUCCESS;
 }
 
-template <int NT, bool kStrictOrder>
+template <int NT, bool kStrictOrder, bool kPersistent>
 cudaError_t launch_nt(AttnParams &p, cudaStream_t stream) {
   using L = Layout<NT>;
   int total = 0;
-  for (int x = 0; x < p.n_pairs; ++x) {
+  if (p.pair_table != nullptr) {
+    // Device-resident table: the caller computed cta_begin / n_qtiles and the total.
+    total = p.total_ctas;
+  }
+  for (int x = 0; x < (p.pair_table != nullptr ? 0 : p.n_pairs); ++x) {
     PairDesc &pd = p.pairs[x];
     if (p.pack_g > 0) {  // n_qtiles counts kv splits in packed mode
       pd.n_qtiles = (pd.kv_len + p.kv_split - 1) / p.kv_split;
@@ -637,7 +759,7 @@ cudaError_t launch_nt(AttnParams &p, cudaStream_t stream) {
       total += pd.n_qtiles * (p.Hq / NT) * p.B;
     }
   }
-  p.total_ctas = total;
+  if (p.pair_table == nullptr) p.total_ctas = total;
   if (total == 0) return cudaSuccess;
   CUtensorMap mq, mk, mv;
   const uint32_t qbox_h = p.pack_g > 0 ? (uint32_t)p.pack_g : 1u;
@@ -647,17 +769,39 @@ cudaError_t launch_nt(AttnParams &p, cudaStream_t stream) {
       !make_map(&mv, p.v, p.B, p.kv_rows_total, p.Hkv, kD, p.v_sb, p.v_ss, p.v_sh))
     return cudaErrorInvalidValue;
   static int configured_device = -1;
+  static int sm_count = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NT, kStrictOrder>,
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NT, kStrictOrder, kPersistent>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::alloc_bytes);
     if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  attn_tc_kernel<NT, kStrictOrder><<<total, L::kThreads, L::alloc_bytes, stream>>>(mq, mk, mv, p);
-  return cudaGetLastError();
+  // Persistent launch: one CTA per SM (shared memory admits only one), each
+  // looping over work items; otherwise one CTA per item.
+  int grid = total;
+  if (p.persistent_ctas > 0) {
+    p.persistent_ctas = sm_count < total ? sm_count : total;
+    grid = p.persistent_ctas;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(L::kThreads);
+  cfg.dynamicSmemBytes = L::alloc_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (p.dep_counters != nullptr) {
+    // CTAs wait on other CTAs' progress counters: they must all be resident.
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<NT, kStrictOrder, kPersistent>, mq, mk, mv, p);
 }
 
 }  // namespace
@@ -682,12 +826,21 @@ bool strict_mma_order() {
   return e != nullptr && e[0] != '\0' && e[0] != '0';
 }
 
+int attn_tc_tiles_per_cta(const AttnParams &p) {
+  return (p.pack_g == 0 && (p.Hq / p.Hkv) % 2 == 0) ? 2 : 1;
+}
+
+template <int NT>
+cudaError_t launch_nt_any(AttnParams &p, cudaStream_t stream, bool strict) {
+  const bool pers = p.persistent_ctas > 0;
+  if (strict) return pers ? launch_nt<NT, true, true>(p, stream) : launch_nt<NT, true, false>(p, stream);
+  return pers ? launch_nt<NT, false, true>(p, stream) : launch_nt<NT, false, false>(p, stream);
+}
+
 cudaError_t launch_attn_tc(AttnParams &p, cudaStream_t stream) {
-  const int g = p.Hq / p.Hkv;
   const bool strict = strict_mma_order();
-  if (p.pack_g == 0 && g % 2 == 0)
-    return strict ? launch_nt<2, true>(p, stream) : launch_nt<2, false>(p, stream);
-  return strict ? launch_nt<1, true>(p, stream) : launch_nt<1, false>(p, stream);
+  if (attn_tc_tiles_per_cta(p) == 2) return launch_nt_any<2>(p, stream, strict);
+  return launch_nt_any<1>(p, stream, strict);
 }
 
 unsigned int attn_tc_read_status(bool clear, cudaError_t *err) {

@@ -38,8 +38,10 @@ struct PairDesc {
   int64_t delta;            // absolute position of q_row0 minus that of kv_row0
   int32_t mode;             // PairMode
   int32_t slot;             // kPartial: workspace slot index
-  int32_t cta_begin;        // filled by the launcher: first block of this pair
+  int32_t cta_begin;        // filled by the launcher: first work item of this pair
   int32_t n_qtiles;         // filled by the launcher
+  int32_t visit;            // Pass-KV, one launch for all steps: visits of this Q piece before
+  int32_t dep_base;         // ... and the base of its progress counters
 };
 
 struct AttnParams {
@@ -61,6 +63,16 @@ struct AttnParams {
   // slot pairs[x].slot + split.  pack_g = 0: one head per tile row block.
   int32_t pack_g;
   int32_t kv_split;
+  // Work items: pairs[] (at most kMaxPairs) or, when pair_table is set, a
+  // device-resident table of n_table pairs (all ring steps of one call).
+  const PairDesc *pair_table;
+  int32_t n_table;
+  // Grid size for a persistent launch (each CTA loops over work items); 0 =
+  // one CTA per work item.
+  int32_t persistent_ctas;
+  // Pass-KV in one launch: per (Q-piece tile, head, batch) count of finished
+  // accumulator updates; an update waits until the count reaches its visit.
+  int32_t *dep_counters;
   OutView out;              // final output (absolute q rows)
   OutView acc;              // Pass-KV fp32 accumulator (absolute q rows)
   OutView part;             // Pass-Q slot 0 (chunk-relative rows)
@@ -98,6 +110,8 @@ cudaError_t launch_merge_2(const Merge2Params &p, cudaStream_t stream);
 
 // True when the tensor-core kernel supports these shapes.
 bool attn_tc_supported(const AttnParams &p);
+// Query tiles (heads) per CTA the tensor-core kernel uses for these shapes.
+int attn_tc_tiles_per_cta(const AttnParams &p);
 
 // Device status words (one per translation unit that has bounded waits).
 unsigned int attn_tc_read_status(bool clear, cudaError_t *err);

@@ -208,9 +208,32 @@ cpattn_status cpattn_prefill_plan(int64_t sq, int64_t skv, int64_t q_base, int n
  * (Pass-Q); Pass-KV then launches once per visiting K/V piece.
  */
 typedef enum { CPATTN_ASSIGN_CONTIGUOUS = 0, CPATTN_ASSIGN_ZIGZAG = 1 } cpattn_assignment;
+
+/*
+ * How the ring steps are launched (bf16, d = 128 tensor-core path; other
+ * shapes always launch per step):
+ *   PER_STEP             one launch per ring step, one CTA per work item;
+ *   PERSISTENT_STEP      one launch per ring step, one CTA per SM looping over
+ *                        the step's work items;
+ *   SINGLE               one persistent launch for all ring steps (the
+ *                        single-GPU form of a device-driven ring): work items
+ *                        keep the ring order, and a Pass-KV accumulator update
+ *                        waits -- bounded, CPATTN_ERR_TIMEOUT if it gives up --
+ *                        until the previous step's update of the same rows has
+ *                        finished.  Launched cooperatively (all CTAs resident).
+ * CPATTN_LAUNCH_DEFAULT is PER_STEP.
+ */
+typedef enum {
+  CPATTN_LAUNCH_PER_STEP = 0,
+  CPATTN_LAUNCH_PERSISTENT_STEP = 1,
+  CPATTN_LAUNCH_SINGLE = 2,
+  CPATTN_LAUNCH_DEFAULT = 0
+} cpattn_launch_mode;
+
 typedef struct {
   int32_t assignment;   /* cpattn_assignment */
-  int32_t reserved[7];  /* zero */
+  int32_t launch;       /* cpattn_launch_mode */
+  int32_t reserved[6];  /* zero */
 } cpattn_prefill_options;
 
 /* cpattn_prefill / _workspace_size / _plan with options (NULL = defaults). */

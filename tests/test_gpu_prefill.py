@@ -117,3 +117,29 @@ def test_prefill_zigzag_assignment(B, name):
         assert d_o <= tol[0] and d_l <= tol[1], (d_o, d_l)
     del q, k, v, base
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("launch", [1, 2], ids=["persistent_step", "single_launch"])
+@pytest.mark.parametrize("name,assignment", [("llama3-8b", 0), ("partial-32k", 0), ("128k", 0),
+                                             ("llama3-8b", 1), ("128k", 1)])
+def test_prefill_launch_modes_match(B, name, assignment, launch):
+    """Persistent CTAs per ring step, and one persistent launch for all ring
+    steps (with Pass-KV accumulator updates ordered by progress counters), give
+    bitwise the same result as one CTA per work item."""
+    from context_ring_attention_cpattn_gb300.workloads import WORKLOADS, make_qkv, sample_rows
+
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w, device="cuda")
+    rows = sample_rows(w, n=min(N_SAMPLE, w.sq, 512))
+    ref_o, ref_l = oracle_rows(q, k, v, rows, q_base=w.q_base, causal=w.causal)
+    for mode in (B.PASS_KV, B.PASS_Q):
+        o0, l0 = B.prefill(q, k, v, w.n_chunks, mode, q_base=w.q_base, causal=w.causal,
+                           assignment=assignment)
+        o1, l1 = B.prefill(q, k, v, w.n_chunks, mode, q_base=w.q_base, causal=w.causal,
+                           assignment=assignment, launch=launch)
+        torch.cuda.synchronize()
+        assert B.device_status() == 0
+        assert torch.equal(o0, o1) and torch.equal(l0, l1), (name, mode)
+        compare(o1, l1, rows, ref_o, ref_l, TOL[w.dtype], f"{name} launch {launch} mode {mode}")
+    del q, k, v
+    torch.cuda.empty_cache()
