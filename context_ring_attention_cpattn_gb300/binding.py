@@ -34,15 +34,15 @@ class PlanEntry(ctypes.Structure):
 
 class PrefillOptions(ctypes.Structure):
     _fields_ = [("assignment", ctypes.c_int32), ("launch", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 6)]
+                ("hold_ordered_waits", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
 
 
 ASSIGN_CONTIGUOUS, ASSIGN_ZIGZAG = 0, 1
 LAUNCH_PER_STEP, LAUNCH_PERSISTENT_STEP, LAUNCH_SINGLE = 0, 1, 2
 
 
-def _opts(assignment: int, launch: int = LAUNCH_PER_STEP):
-    return ctypes.byref(PrefillOptions(int(assignment), int(launch)))
+def _opts(assignment: int, launch: int = LAUNCH_PER_STEP, hold_ordered_waits: bool = False):
+    return ctypes.byref(PrefillOptions(int(assignment), int(launch), int(bool(hold_ordered_waits))))
 
 
 class ProfileRecord(ctypes.Structure):
@@ -188,8 +188,10 @@ def workspace_size(q, k, n_chunks: int, mode: int, q_base: int = 0, causal: bool
 
 def prefill(q, k, v, n_chunks: int, mode: int, q_base: int = 0, causal: bool = True, scale=None,
             out=None, lse=None, workspace=None, out_dtype=None, stream=None,
-            assignment: int = ASSIGN_CONTIGUOUS, launch: int = LAUNCH_PER_STEP):
-    """CP prefill of one attention layer on one GPU; see cpattn_prefill_ex."""
+            assignment: int = ASSIGN_CONTIGUOUS, launch: int = LAUNCH_PER_STEP,
+            hold_ordered_waits: bool = False):
+    """CP prefill of one attention layer on one GPU; see cpattn_prefill_ex.
+    ``hold_ordered_waits`` exists only to test failure detection."""
     import torch
 
     B, S, H, D = q.shape
@@ -206,7 +208,8 @@ def prefill(q, k, v, n_chunks: int, mode: int, q_base: int = 0, causal: bool = T
     _check(lib().cpattn_prefill_ex(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
                                    int(q_base), int(n_chunks), int(mode), int(bool(causal)),
                                    float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(), ws_ptr,
-                                   ws_len, _opts(assignment, launch), _stream(stream)),
+                                   ws_len, _opts(assignment, launch, hold_ordered_waits),
+                                   _stream(stream)),
            "cpattn_prefill_ex")
     return out, lse
 

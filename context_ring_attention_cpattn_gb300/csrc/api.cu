@@ -468,6 +468,7 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
       p.persistent_ctas = 1;
       if (pl.mode == CPATTN_PASS_KV && pl.need_acc) {
         p.dep_counters = reinterpret_cast<int32_t *>(ws + wl.counters);
+        p.dep_hold = (opts != nullptr && opts->hold_ordered_waits != 0) ? (1 << 28) : 0;
         if (cudaMemsetAsync(p.dep_counters, 0, wl.n_counters * sizeof(int32_t), st) != cudaSuccess)
           return CPATTN_ERR_CUDA;
       }
@@ -475,6 +476,7 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
       p.pair_table = nullptr;
       p.n_table = 0;
       p.dep_counters = nullptr;
+      p.dep_hold = 0;
       p.persistent_ctas = 0;
     }
   }

@@ -641,22 +641,29 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
       if (kPersistent && p.dep_counters != nullptr && G == 0 &&
           (pd.mode == kAccInit || pd.mode == kAccMerge || pd.mode == kAccFinal))
         dep = p.dep_counters + pd.dep_base + ((int64_t)it.qt * p.Hq + head) * p.B + it.b;
+      // Each of the tile's 4 warps adds 1 when its rows are written, so the
+      // rows' earlier visits are done once the count reaches 4 * visit.  Every
+      // warp waits and publishes for itself: no barrier spans warps whose
+      // abort decisions may differ.
       if (dep != nullptr && pd.visit > 0) {
-        if (warp % 4 == 0 && lane == 0) {
+        int got = 1;
+        if (lane == 0) {
+          const int target = 4 * pd.visit + p.dep_hold;
           const unsigned long long t0 = global_ns();
           for (uint32_t spin = 0;; ++spin) {
             int v;
             asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(dep) : "memory");
-            if (v >= pd.visit) break;
+            if (v >= target) break;
             if ((spin & 63u) == 63u && (*abort_flag || global_ns() - t0 > kWaitNs)) {
               *abort_flag = 1;
               atomicOr(&g_attn_tc_status, 1u);
+              got = 0;
               break;
             }
           }
         }
-        asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");
-        if (*abort_flag) { ok = false; break; }
+        __syncwarp();
+        if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
       }
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
@@ -683,10 +690,10 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
         if (lane == 0) mbar_arrive(bar(L::b_ofree + t));
       }
       if (dep != nullptr && pd.mode != kAccFinal) {
-        asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");
-        if (warp % 4 == 0 && lane == 0) {
+        __syncwarp();
+        if (lane == 0) {
           __threadfence();
-          asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(dep), "r"(pd.visit + 1) : "memory");
+          asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(dep) : "memory");
         }
       }
       g += n_kv;

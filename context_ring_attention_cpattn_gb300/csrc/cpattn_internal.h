@@ -70,9 +70,12 @@ struct AttnParams {
   // Grid size for a persistent launch (each CTA loops over work items); 0 =
   // one CTA per work item.
   int32_t persistent_ctas;
-  // Pass-KV in one launch: per (Q-piece tile, head, batch) count of finished
-  // accumulator updates; an update waits until the count reaches its visit.
+  // Pass-KV in one launch: per (Q-piece tile, head, batch) count of warps
+  // that finished an accumulator update (4 per update); an update waits until
+  // the count reaches 4 * its visit (+ dep_hold, nonzero only to make the
+  // bounded wait run out when testing failure detection).
   int32_t *dep_counters;
+  int32_t dep_hold;
   OutView out;              // final output (absolute q rows)
   OutView acc;              // Pass-KV fp32 accumulator (absolute q rows)
   OutView part;             // Pass-Q slot 0 (chunk-relative rows)

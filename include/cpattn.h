@@ -230,10 +230,19 @@ typedef enum {
   CPATTN_LAUNCH_DEFAULT = 0
 } cpattn_launch_mode;
 
+/*
+ * hold_ordered_waits -- failure-detection test only (zero in normal use).
+ * Nonzero makes every ordered Pass-KV accumulator update of a SINGLE launch
+ * wait for a progress count that is never reached: the wait gives up after
+ * its bound (2 s), cpattn_device_status() then reports CPATTN_ERR_TIMEOUT, O
+ * and LSE are undefined, and the CUDA context stays usable.  Ignored by the
+ * other launch modes and by Pass-Q, which have no ordered updates.
+ */
 typedef struct {
-  int32_t assignment;   /* cpattn_assignment */
-  int32_t launch;       /* cpattn_launch_mode */
-  int32_t reserved[6];  /* zero */
+  int32_t assignment;          /* cpattn_assignment */
+  int32_t launch;              /* cpattn_launch_mode */
+  int32_t hold_ordered_waits;  /* see above; 0 */
+  int32_t reserved[5];         /* zero */
 } cpattn_prefill_options;
 
 /* cpattn_prefill / _workspace_size / _plan with options (NULL = defaults). */

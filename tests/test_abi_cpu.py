@@ -33,6 +33,26 @@ def test_header_and_binding_agree():
     assert declared_functions() == sorted(B.EXPORTED)
 
 
+def declared_struct_fields(name):
+    """Field names of a typedef'd struct in the header, in order."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct \{([^}]*)\}\s*" + name + ";", text).group(1)
+    fields = []
+    for decl in filter(None, (d.strip() for d in body.split(";"))):
+        names = decl.split(None, 1)[1]          # drop the type
+        fields += [re.sub(r"[*\s]|\[\d+\]", "", n) for n in names.split(",")]
+    return fields
+
+
+@pytest.mark.parametrize("cname,pyname", [("cpattn_tensor", "CpattnTensor"),
+                                          ("cpattn_plan_entry", "PlanEntry"),
+                                          ("cpattn_prefill_options", "PrefillOptions"),
+                                          ("cpattn_profile_record", "ProfileRecord")])
+def test_binding_structs_match_header(cname, pyname):
+    fields = [f[0] for f in getattr(B, pyname)._fields_]
+    assert declared_struct_fields(cname) == fields
+
+
 def test_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name

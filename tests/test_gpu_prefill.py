@@ -143,3 +143,30 @@ def test_prefill_launch_modes_match(B, name, assignment, launch):
         compare(o1, l1, rows, ref_o, ref_l, TOL[w.dtype], f"{name} launch {launch} mode {mode}")
     del q, k, v
     torch.cuda.empty_cache()
+
+
+def test_single_launch_wait_runs_out(B):
+    """Failure detection without a device fault: with hold_ordered_waits every
+    ordered Pass-KV accumulator update of a single launch waits for a progress
+    count that nothing reaches.  The bounded wait gives up, the host reads
+    CPATTN_ERR_TIMEOUT from cpattn_device_status, and the context stays usable:
+    the next call is correct and reports no error."""
+    import time
+
+    from context_ring_attention_cpattn_gb300.workloads import WORKLOADS, make_qkv
+
+    w = WORKLOADS["llama3-8b"]
+    q, k, v = make_qkv(w, device="cuda")
+    o_ref, l_ref = B.prefill(q, k, v, w.n_chunks, B.PASS_KV)
+    torch.cuda.synchronize()
+    assert B.device_status() == 0
+    t0 = time.time()
+    B.prefill(q, k, v, w.n_chunks, B.PASS_KV, launch=B.LAUNCH_SINGLE, hold_ordered_waits=True)
+    assert B.device_status() == 5   # CPATTN_ERR_TIMEOUT; synchronizes first
+    elapsed = time.time() - t0
+    assert 1.0 < elapsed < 60.0, elapsed
+    assert B.device_status() == 0   # cleared by the previous read
+    o, lse = B.prefill(q, k, v, w.n_chunks, B.PASS_KV, launch=B.LAUNCH_SINGLE)
+    torch.cuda.synchronize()
+    assert B.device_status() == 0
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
