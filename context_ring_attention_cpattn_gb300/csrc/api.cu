@@ -17,6 +17,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <functional>
 #include <new>
 #include <vector>
 
@@ -359,10 +360,15 @@ int launch_mode_of(const cpattn_prefill_options *opts) {
   return opts ? opts->launch : CPATTN_LAUNCH_DEFAULT;
 }
 
+// Called (at enqueue time, on the host) once the work that finalises output
+// rows [row0, row0 + rows) has been enqueued on the stream.
+using FinalRowsFn = std::function<cudaError_t(int64_t row0, int64_t rows)>;
+
 cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const cpattn_tensor *v,
                            int64_t q_base, int n_chunks, int mode, int causal, float scale,
                            cpattn_tensor *o, float *lse, void *workspace, size_t ws_bytes,
-                           const cpattn_prefill_options *opts, cudaStream_t st) {
+                           const cpattn_prefill_options *opts, cudaStream_t st,
+                           const FinalRowsFn *on_final = nullptr) {
   cpattn_status s = check_qkv(q, k, v);
   if (s != CPATTN_OK) return s;
   if ((s = check_out(o, lse, q)) != CPATTN_OK) return s;
@@ -480,9 +486,57 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
       p.persistent_ctas = 0;
     }
   }
+  const bool per_step = !(lmode == CPATTN_LAUNCH_SINGLE && attn_tc_supported(p));
+  // Pass-Q merge of partials, and empty rows of chunks no key reaches: one
+  // launch for the listed pieces.
+  MergeNParams mp;
+  memset(&mp, 0, sizeof(mp));
+  mp.B = (int32_t)q->b;
+  mp.H = (int32_t)q->h;
+  mp.D = (int32_t)q->d;
+  mp.chunk_rows = (int32_t)pl.Cq;
+  mp.out = p.out;
+  mp.part = p.part;
+  mp.part_o_stride = p.part_o_stride;
+  mp.part_lse_stride = p.part_lse_stride;
+  const double row_bytes = (double)q->b * pl.Cq * q->h * (q->d * 4.0 + 4.0);
+  const double out_bytes = (double)q->b * pl.Cq * q->h * (q->d * elem_bytes(o->dtype) + 4.0);
+  auto needs_merge_launch = [&](int i) {
+    return (pl.mode == CPATTN_PASS_Q && pl.count[i] >= 2) || pl.count[i] == 0;
+  };
+  auto merge_pieces = [&](std::vector<int> pieces) -> cpattn_status {
+    // Items with the most partials first (longest CTAs first).
+    std::stable_sort(pieces.begin(), pieces.end(),
+                     [&](int a, int b) { return pl.count[a] > pl.count[b]; });
+    mp.n_items = 0;
+    double bytes = 0.0;
+    for (int i : pieces) {
+      const bool merge = pl.count[i] >= 2;
+      mp.item_row0[mp.n_items] = (int32_t)(i * pl.Cq);
+      mp.item_slot0[mp.n_items] = merge ? pl.slot0[i] : 0;
+      mp.item_count[mp.n_items] = merge ? pl.count[i] : 0;
+      bytes += (merge ? pl.count[i] * row_bytes : 0.0) + out_bytes;
+      ++mp.n_items;
+    }
+    if (mp.n_items == 0) return CPATTN_OK;
+    prof_before(st);
+    cudaError_t e = launch_merge_n(mp, st);
+    prof_after(st, CPATTN_KERNEL_MERGEN, bytes);
+    if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+    for (int i : pieces)
+      if (per_step && on_final != nullptr && (*on_final)(i * pl.Cq, pl.Cq) != cudaSuccess)
+        return CPATTN_ERR_CUDA;
+    return CPATTN_OK;
+  };
+  // With a finality callback, a piece's Pass-Q merge runs right after the
+  // launch that produced its last partial, so its rows can leave early.
+  std::vector<int> last_launch(pl.P, -1);
+  for (const auto &e : pl.entries)
+    if (e.role == CPATTN_ROLE_PARTIAL) last_launch[e.q_chunk] = std::max(last_launch[e.q_chunk], e.launch);
+  std::vector<bool> merged(pl.P, false);
+
   // One launch per ring step (two per step for zigzag Pass-KV, one per
   // visiting K/V piece).
-  const bool per_step = !(lmode == CPATTN_LAUNCH_SINGLE && attn_tc_supported(p));
   p.persistent_ctas = lmode == CPATTN_LAUNCH_PERSISTENT_STEP ? 1 : 0;
   size_t e0 = 0;
   for (int l = 0; l < pl.n_launches && per_step; ++l) {
@@ -494,43 +548,29 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
     p.n_pairs = (int32_t)items.size();
     for (size_t x = 0; x < items.size(); ++x) p.pairs[x] = items[x];
     if (launch_attn(p, st, q) != cudaSuccess) return CPATTN_ERR_CUDA;
+    if (on_final != nullptr) {
+      std::vector<int> ready;
+      for (size_t x = e0; x < e1; ++x) {
+        const cpattn_plan_entry &e = pl.entries[x];
+        if (e.role == CPATTN_ROLE_STORE || e.role == CPATTN_ROLE_ACC_FINAL) {
+          if ((*on_final)(e.q_chunk * pl.Cq, pl.Cq) != cudaSuccess) return CPATTN_ERR_CUDA;
+        } else if (e.role == CPATTN_ROLE_PARTIAL && last_launch[e.q_chunk] == l &&
+                   needs_merge_launch(e.q_chunk) && !merged[e.q_chunk]) {
+          ready.push_back(e.q_chunk);
+          merged[e.q_chunk] = true;
+        }
+      }
+      if ((s = merge_pieces(ready)) != CPATTN_OK) return s;
+    }
     e0 = e1;
   }
 
-  // Pass-Q merge of partials, and empty rows of chunks no key reaches.
-  MergeNParams mp;
-  memset(&mp, 0, sizeof(mp));
-  mp.B = (int32_t)q->b;
-  mp.H = (int32_t)q->h;
-  mp.D = (int32_t)q->d;
-  mp.chunk_rows = (int32_t)pl.Cq;
-  mp.out = p.out;
-  mp.part = p.part;
-  mp.part_o_stride = p.part_o_stride;
-  mp.part_lse_stride = p.part_lse_stride;
-  double bytes = 0.0;
-  const double row_bytes = (double)q->b * pl.Cq * q->h * (q->d * 4.0 + 4.0);
-  const double out_bytes = (double)q->b * pl.Cq * q->h * (q->d * elem_bytes(o->dtype) + 4.0);
-  // Items with the most partials first (longest CTAs first).
-  std::vector<int> order(pl.P);
-  for (int i = 0; i < pl.P; ++i) order[i] = i;
-  std::stable_sort(order.begin(), order.end(),
-                   [&](int a, int b) { return pl.count[a] > pl.count[b]; });
-  for (int i : order) {
-    const bool merge = pl.mode == CPATTN_PASS_Q && pl.count[i] >= 2;
-    if (!merge && pl.count[i] != 0) continue;
-    mp.item_row0[mp.n_items] = (int32_t)(i * pl.Cq);
-    mp.item_slot0[mp.n_items] = merge ? pl.slot0[i] : 0;
-    mp.item_count[mp.n_items] = merge ? pl.count[i] : 0;
-    bytes += (merge ? pl.count[i] * row_bytes : 0.0) + out_bytes;
-    ++mp.n_items;
-  }
-  if (mp.n_items > 0) {
-    prof_before(st);
-    cudaError_t e = launch_merge_n(mp, st);
-    prof_after(st, CPATTN_KERNEL_MERGEN, bytes);
-    if (e != cudaSuccess) return CPATTN_ERR_CUDA;
-  }
+  std::vector<int> rest;
+  for (int i = 0; i < pl.P; ++i)
+    if (needs_merge_launch(i) && !merged[i]) rest.push_back(i);
+  if ((s = merge_pieces(rest)) != CPATTN_OK) return s;
+  if (!per_step && on_final != nullptr && (*on_final)(0, q->s) != cudaSuccess)
+    return CPATTN_ERR_CUDA;
   return CPATTN_OK;
 }
 
@@ -901,6 +941,19 @@ cpattn_status cpattn_prefill_host_scratch_size(const cpattn_tensor *q, const cpa
   return CPATTN_OK;
 }
 
+// Side stream and events of one host-buffer call, released on every path out.
+struct CopyStream {
+  cudaStream_t s = nullptr;
+  std::vector<cudaEvent_t> events;
+  ~CopyStream() {
+    if (s != nullptr) {
+      cudaStreamSynchronize(s);
+      cudaStreamDestroy(s);
+    }
+    for (auto ev : events) cudaEventDestroy(ev);
+  }
+};
+
 cpattn_status cpattn_prefill_host(const cpattn_tensor *q, const cpattn_tensor *k,
                                   const cpattn_tensor *v, int64_t q_base, int n_chunks, int mode,
                                   int causal, float scale, cpattn_tensor *o, float *lse,
@@ -935,12 +988,34 @@ cpattn_status cpattn_prefill_host(const cpattn_tensor *q, const cpattn_tensor *k
         cudaMemcpyAsync(dk.data, k->data, tensor_bytes(k), cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemcpyAsync(dv.data, v->data, tensor_bytes(v), cudaMemcpyHostToDevice, st) != cudaSuccess)
       return CPATTN_ERR_CUDA;
-    s = prefill_impl(&dq, &dk, &dv, q_base, n_chunks, mode, causal, scale, &dout, dlse, ws,
-                     ws_bytes, nullptr, st);
-    if (s != CPATTN_OK) return s;
-    if (cudaMemcpyAsync(o->data, dout.data, o_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaMemcpyAsync(lse, dlse, lse_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    // Output rows go back to the host on a second stream as soon as the
+    // launch that finalises them has been enqueued (a Pass-KV piece after its
+    // last ring step, a Pass-Q piece after its merge), overlapping the copies
+    // with the remaining ring steps.
+    CopyStream cs;
+    if (cudaStreamCreateWithFlags(&cs.s, cudaStreamNonBlocking) != cudaSuccess)
       return CPATTN_ERR_CUDA;
+    const int64_t row_bytes = q->h * q->d * elem_bytes(o->dtype);
+    const FinalRowsFn on_final = [&](int64_t row0, int64_t rows) -> cudaError_t {
+      cudaEvent_t ev;
+      cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+      if (e != cudaSuccess) return e;
+      cs.events.push_back(ev);
+      if ((e = cudaEventRecord(ev, st)) != cudaSuccess) return e;
+      if ((e = cudaStreamWaitEvent(cs.s, ev, 0)) != cudaSuccess) return e;
+      // O [b, s, h, d]: one block of rows per batch entry.
+      e = cudaMemcpy2DAsync(static_cast<uint8_t *>(o->data) + row0 * row_bytes, q->s * row_bytes,
+                            static_cast<uint8_t *>(dout.data) + row0 * row_bytes, q->s * row_bytes,
+                            rows * row_bytes, q->b, cudaMemcpyDeviceToHost, cs.s);
+      if (e != cudaSuccess) return e;
+      // LSE [b, h, s]: one run of rows per (batch, head).
+      return cudaMemcpy2DAsync(lse + row0, q->s * 4, dlse + row0, q->s * 4, rows * 4, q->b * q->h,
+                               cudaMemcpyDeviceToHost, cs.s);
+    };
+    s = prefill_impl(&dq, &dk, &dv, q_base, n_chunks, mode, causal, scale, &dout, dlse, ws,
+                     ws_bytes, nullptr, st, &on_final);
+    if (s != CPATTN_OK) return s;
+    if (cudaStreamSynchronize(cs.s) != cudaSuccess) return CPATTN_ERR_CUDA;
     return cudaStreamSynchronize(st) == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
   } catch (...) {
     return CPATTN_ERR_INVALID_ARG;

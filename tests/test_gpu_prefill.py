@@ -78,19 +78,24 @@ def test_prefill_edge_cases(B, case, mode):
     compare(o, lse, rows, ref_o, ref_l, TOL[dt], f"edge {case} mode {mode}")
 
 
-def test_prefill_host_entry_point(B):
-    """The host-buffer entry point gives the same result as the device one."""
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("name,batch", [("llama3-8b", 1), ("partial-32k", 1), ("partial-32k", 2)])
+def test_prefill_host_entry_point(B, mode, name, batch):
+    """The host-buffer entry point (output rows copied back piece by piece as
+    the ring finalises them) gives the same result as the device one."""
+    import dataclasses
+
     from context_ring_attention_cpattn_gb300.workloads import WORKLOADS, make_qkv
 
-    w = WORKLOADS["llama3-8b"]
+    w = dataclasses.replace(WORKLOADS[name], batch=batch)
     q, k, v = make_qkv(w, device="cuda")
-    o_ref, l_ref = B.prefill(q, k, v, w.n_chunks, B.PASS_KV)
+    o_ref, l_ref = B.prefill(q, k, v, w.n_chunks, mode, q_base=w.q_base)
     qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
-    oh = torch.empty_like(qh).pin_memory()
-    lh = torch.empty((1, w.hq, w.sq), dtype=torch.float32).pin_memory()
-    scratch = torch.empty(B.host_scratch_size(qh, kh, w.n_chunks, B.PASS_KV), dtype=torch.uint8,
-                          device="cuda")
-    B.prefill_host(qh, kh, vh, w.n_chunks, B.PASS_KV, oh, lh, scratch)
+    oh = torch.full_like(qh, float("nan")).pin_memory()
+    lh = torch.full((batch, w.hq, w.sq), float("nan"), dtype=torch.float32).pin_memory()
+    scratch = torch.empty(B.host_scratch_size(qh, kh, w.n_chunks, mode, q_base=w.q_base),
+                          dtype=torch.uint8, device="cuda")
+    B.prefill_host(qh, kh, vh, w.n_chunks, mode, oh, lh, scratch, q_base=w.q_base)
     assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())
 
 
