@@ -363,12 +363,15 @@ int launch_mode_of(const cpattn_prefill_options *opts) {
 // Called (at enqueue time, on the host) once the work that finalises output
 // rows [row0, row0 + rows) has been enqueued on the stream.
 using FinalRowsFn = std::function<cudaError_t(int64_t row0, int64_t rows)>;
+// Called before a launch that reads Q piece q_piece and K/V piece kv_piece.
+using InputsFn = std::function<cudaError_t(int q_piece, int kv_piece)>;
 
 cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const cpattn_tensor *v,
                            int64_t q_base, int n_chunks, int mode, int causal, float scale,
                            cpattn_tensor *o, float *lse, void *workspace, size_t ws_bytes,
                            const cpattn_prefill_options *opts, cudaStream_t st,
-                           const FinalRowsFn *on_final = nullptr) {
+                           const FinalRowsFn *on_final = nullptr,
+                           const InputsFn *on_inputs = nullptr) {
   cpattn_status s = check_qkv(q, k, v);
   if (s != CPATTN_OK) return s;
   if ((s = check_out(o, lse, q)) != CPATTN_OK) return s;
@@ -545,9 +548,26 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
     if (e1 == e0) continue;
     std::vector<PairDesc> items;
     launch_items(e0, e1, items);
-    p.n_pairs = (int32_t)items.size();
-    for (size_t x = 0; x < items.size(); ++x) p.pairs[x] = items[x];
-    if (launch_attn(p, st, q) != cudaSuccess) return CPATTN_ERR_CUDA;
+    if (on_inputs != nullptr && l == 0) {
+      // Inputs arrive piece by piece: the first ring step runs one pair per
+      // launch, each as soon as its pieces are in (its pairs touch disjoint
+      // output rows, so splitting the launch changes no arithmetic).
+      for (const PairDesc &pd : items) {
+        if ((*on_inputs)(pd.q_row0 / (int32_t)pl.Cq, pd.kv_row0 / (int32_t)pl.C) != cudaSuccess)
+          return CPATTN_ERR_CUDA;
+        p.n_pairs = 1;
+        p.pairs[0] = pd;
+        if (launch_attn(p, st, q) != cudaSuccess) return CPATTN_ERR_CUDA;
+      }
+    } else {
+      for (const PairDesc &pd : items)
+        if (on_inputs != nullptr &&
+            (*on_inputs)(pd.q_row0 / (int32_t)pl.Cq, pd.kv_row0 / (int32_t)pl.C) != cudaSuccess)
+          return CPATTN_ERR_CUDA;
+      p.n_pairs = (int32_t)items.size();
+      for (size_t x = 0; x < items.size(); ++x) p.pairs[x] = items[x];
+      if (launch_attn(p, st, q) != cudaSuccess) return CPATTN_ERR_CUDA;
+    }
     if (on_final != nullptr) {
       std::vector<int> ready;
       for (size_t x = e0; x < e1; ++x) {
@@ -941,7 +961,7 @@ cpattn_status cpattn_prefill_host_scratch_size(const cpattn_tensor *q, const cpa
   return CPATTN_OK;
 }
 
-// Side stream and events of one host-buffer call, released on every path out.
+// Side streams and events of one host-buffer call, released on every path out.
 struct CopyStream {
   cudaStream_t s = nullptr;
   std::vector<cudaEvent_t> events;
@@ -951,6 +971,12 @@ struct CopyStream {
       cudaStreamDestroy(s);
     }
     for (auto ev : events) cudaEventDestroy(ev);
+  }
+  cudaError_t record(cudaStream_t on, cudaEvent_t *out) {
+    cudaError_t e = cudaEventCreateWithFlags(out, cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+    events.push_back(*out);
+    return cudaEventRecord(*out, on);
   }
 };
 
@@ -984,38 +1010,75 @@ cpattn_status cpattn_prefill_host(const cpattn_tensor *q, const cpattn_tensor *k
     float *dlse = reinterpret_cast<float *>(take(lse_bytes));
     void *ws = base + off;
     const size_t ws_bytes = scratch_bytes - off;
-    if (cudaMemcpyAsync(dq.data, q->data, tensor_bytes(q), cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(dk.data, k->data, tensor_bytes(k), cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(dv.data, v->data, tensor_bytes(v), cudaMemcpyHostToDevice, st) != cudaSuccess)
+    if (q->s == 0) return CPATTN_OK;
+    Plan pl;
+    if ((s = build_plan(q->s, k->s, q_base, n_chunks, mode, causal, CPATTN_ASSIGN_CONTIGUOUS, pl)) !=
+        CPATTN_OK)
+      return s;
+    // Inputs come in on one side stream (K and V first, then Q a piece at a
+    // time) while the first ring step starts on each piece as it lands;
+    // output rows go back on another as soon as the launch that finalises
+    // them has been enqueued (a Pass-KV piece after its last ring step, a
+    // Pass-Q piece after its merge), overlapping both directions of copies
+    // with the ring.
+    CopyStream up, down;
+    if (cudaStreamCreateWithFlags(&up.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&down.s, cudaStreamNonBlocking) != cudaSuccess)
       return CPATTN_ERR_CUDA;
-    // Output rows go back to the host on a second stream as soon as the
-    // launch that finalises them has been enqueued (a Pass-KV piece after its
-    // last ring step, a Pass-Q piece after its merge), overlapping the copies
-    // with the remaining ring steps.
-    CopyStream cs;
-    if (cudaStreamCreateWithFlags(&cs.s, cudaStreamNonBlocking) != cudaSuccess)
+    // The caller's stream may hold earlier work on the scratch buffer.
+    cudaEvent_t ev_start, ev_kv;
+    if (up.record(st, &ev_start) != cudaSuccess || cudaStreamWaitEvent(up.s, ev_start, 0) != cudaSuccess)
       return CPATTN_ERR_CUDA;
+    if (cudaMemcpyAsync(dk.data, k->data, tensor_bytes(k), cudaMemcpyHostToDevice, up.s) != cudaSuccess ||
+        cudaMemcpyAsync(dv.data, v->data, tensor_bytes(v), cudaMemcpyHostToDevice, up.s) != cudaSuccess ||
+        up.record(up.s, &ev_kv) != cudaSuccess)
+      return CPATTN_ERR_CUDA;
+    const int64_t q_row_bytes = q->h * q->d * elem_bytes(q->dtype);
+    std::vector<cudaEvent_t> ev_q(pl.P);
+    for (int i = 0; i < pl.P; ++i) {
+      if (cudaMemcpy2DAsync(static_cast<uint8_t *>(dq.data) + i * pl.Cq * q_row_bytes,
+                            q->s * q_row_bytes,
+                            static_cast<const uint8_t *>(q->data) + i * pl.Cq * q_row_bytes,
+                            q->s * q_row_bytes, pl.Cq * q_row_bytes, q->b, cudaMemcpyHostToDevice,
+                            up.s) != cudaSuccess ||
+          up.record(up.s, &ev_q[i]) != cudaSuccess)
+        return CPATTN_ERR_CUDA;
+    }
+    std::vector<bool> have_q(pl.P, false);
+    bool have_kv = false;
+    const InputsFn on_inputs = [&](int q_piece, int kv_piece) -> cudaError_t {
+      (void)kv_piece;
+      cudaError_t e = cudaSuccess;
+      if (!have_kv && (e = cudaStreamWaitEvent(st, ev_kv, 0)) != cudaSuccess) return e;
+      have_kv = true;
+      if (q_piece >= 0 && q_piece < pl.P && !have_q[q_piece]) {
+        if ((e = cudaStreamWaitEvent(st, ev_q[q_piece], 0)) != cudaSuccess) return e;
+        have_q[q_piece] = true;
+      }
+      return e;
+    };
     const int64_t row_bytes = q->h * q->d * elem_bytes(o->dtype);
     const FinalRowsFn on_final = [&](int64_t row0, int64_t rows) -> cudaError_t {
       cudaEvent_t ev;
-      cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+      cudaError_t e = down.record(st, &ev);
       if (e != cudaSuccess) return e;
-      cs.events.push_back(ev);
-      if ((e = cudaEventRecord(ev, st)) != cudaSuccess) return e;
-      if ((e = cudaStreamWaitEvent(cs.s, ev, 0)) != cudaSuccess) return e;
+      if ((e = cudaStreamWaitEvent(down.s, ev, 0)) != cudaSuccess) return e;
       // O [b, s, h, d]: one block of rows per batch entry.
       e = cudaMemcpy2DAsync(static_cast<uint8_t *>(o->data) + row0 * row_bytes, q->s * row_bytes,
                             static_cast<uint8_t *>(dout.data) + row0 * row_bytes, q->s * row_bytes,
-                            rows * row_bytes, q->b, cudaMemcpyDeviceToHost, cs.s);
+                            rows * row_bytes, q->b, cudaMemcpyDeviceToHost, down.s);
       if (e != cudaSuccess) return e;
       // LSE [b, h, s]: one run of rows per (batch, head).
       return cudaMemcpy2DAsync(lse + row0, q->s * 4, dlse + row0, q->s * 4, rows * 4, q->b * q->h,
-                               cudaMemcpyDeviceToHost, cs.s);
+                               cudaMemcpyDeviceToHost, down.s);
     };
     s = prefill_impl(&dq, &dk, &dv, q_base, n_chunks, mode, causal, scale, &dout, dlse, ws,
-                     ws_bytes, nullptr, st, &on_final);
+                     ws_bytes, nullptr, st, &on_final, &on_inputs);
     if (s != CPATTN_OK) return s;
-    if (cudaStreamSynchronize(cs.s) != cudaSuccess) return CPATTN_ERR_CUDA;
+    // Rows no launch reads (a piece no key reaches) still wait for every input.
+    for (int i = 0; i < pl.P; ++i)
+      if (on_inputs(i, 0) != cudaSuccess) return CPATTN_ERR_CUDA;
+    if (cudaStreamSynchronize(down.s) != cudaSuccess) return CPATTN_ERR_CUDA;
     return cudaStreamSynchronize(st) == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
   } catch (...) {
     return CPATTN_ERR_INVALID_ARG;
