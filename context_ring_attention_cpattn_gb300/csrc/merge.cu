@@ -167,6 +167,99 @@ __global__ void __launch_bounds__(kWarps * 32) mergen_kernel(const __grid_consta
   }
 }
 
+// Few rows, many partials each (decode: a handful of query rows, one
+// partial per split-KV piece of every chunk): one CTA per (row, item); warp w
+// runs the same online merge over partials w, w + kWarps, w + 2 kWarps, ...,
+// and warp 0 then combines the warps' (max, sum, O) states in shared memory.
+// Every load round keeps kInFlight partials per warp, kWarps * kInFlight per
+// row, in flight.
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32)
+    mergen_split_kernel(const __grid_constant__ MergeNParams p) {
+  constexpr int E = D / 32;
+  constexpr int kInFlight = 4;
+  __shared__ float s_acc[kWarps][D];
+  __shared__ float s_m[kWarps], s_sum[kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int item = blockIdx.y;
+  const int count = p.item_count[item];
+  const int slot0 = p.item_slot0[item];
+  const int64_t r = blockIdx.x;  // the grid has one CTA per row
+  const int h = (int)(r % p.H);
+  const int64_t s = (r / p.H) % p.chunk_rows;
+  const int b = (int)(r / ((int64_t)p.H * p.chunk_rows));
+  const float *lse0 = p.part.lse + (int64_t)slot0 * p.part_lse_stride + (int64_t)b * p.part.lb +
+                      (int64_t)h * p.part.lh + s;
+  const float *o0 = reinterpret_cast<const float *>(p.part.o) + (int64_t)slot0 * p.part_o_stride +
+                    (int64_t)b * p.part.sb + s * p.part.ss + (int64_t)h * p.part.sh + lane * E;
+  float m = -INFINITY, sum = 0.f, acc[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) acc[i] = 0.f;
+  for (int j0 = warp; j0 < count; j0 += kWarps * kInFlight) {
+    float l[kInFlight], v[kInFlight][E];
+#pragma unroll
+    for (int x = 0; x < kInFlight; ++x) {
+      const int j = j0 + x * kWarps;
+      if (j < count) {
+        l[x] = lse0[(int64_t)j * p.part_lse_stride];
+        load_f32<E>(o0 + (int64_t)j * p.part_o_stride, 0, v[x]);
+      } else {
+        l[x] = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < E; ++i) v[x][i] = 0.f;
+      }
+    }
+    float mg = l[0];
+#pragma unroll
+    for (int x = 1; x < kInFlight; ++x) mg = fmaxf(mg, l[x]);
+    const float m_new = fmaxf(m, mg);
+    if (m_new == -INFINITY) continue;
+    const float c = expf(m - m_new);
+    sum *= c;
+#pragma unroll
+    for (int i = 0; i < E; ++i) acc[i] *= c;
+#pragma unroll
+    for (int x = 0; x < kInFlight; ++x) {
+      const float e = expf(l[x] - m_new);
+      sum += e;
+#pragma unroll
+      for (int i = 0; i < E; ++i) acc[i] = fmaf(e, v[x][i], acc[i]);
+    }
+    m = m_new;
+  }
+#pragma unroll
+  for (int i = 0; i < E; ++i) s_acc[warp][lane * E + i] = acc[i];
+  if (lane == 0) {
+    s_m[warp] = m;
+    s_sum[warp] = sum;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, s_m[w]);
+  float tot = 0.f, out[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) out[i] = 0.f;
+  float lse_out = -INFINITY;
+  if (mx != -INFINITY) {
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float c = s_m[w] == -INFINITY ? 0.f : expf(s_m[w] - mx);
+      tot = fmaf(c, s_sum[w], tot);
+#pragma unroll
+      for (int i = 0; i < E; ++i) out[i] = fmaf(c, s_acc[w][lane * E + i], out[i]);
+    }
+    const float inv = 1.f / tot;
+#pragma unroll
+    for (int i = 0; i < E; ++i) out[i] *= inv;
+    lse_out = mx + logf(tot);
+  }
+  const int64_t abs_row = (int64_t)p.item_row0[item] + s;
+  store_vals<E>(view_row(p.out, b, abs_row, h), p.out.f32, lane * E, out);
+  if (lane == 0) *view_lse(p.out, b, abs_row, h) = lse_out;
+}
+
 }  // namespace
 
 cudaError_t launch_merge_2(const Merge2Params &p, cudaStream_t stream) {
@@ -187,6 +280,21 @@ cudaError_t launch_merge_2(const Merge2Params &p, cudaStream_t stream) {
 cudaError_t launch_merge_n(const MergeNParams &p, cudaStream_t stream) {
   const int64_t n_rows = (int64_t)p.B * p.chunk_rows * p.H;
   if (n_rows == 0 || p.n_items == 0) return cudaSuccess;
+  int max_count = 0;
+  for (int x = 0; x < p.n_items; ++x) max_count = p.item_count[x] > max_count ? p.item_count[x] : max_count;
+  // A row per CTA when rows are few and partials many (the row-per-warp grid
+  // would leave most SMs idle and walk each row's partials serially).
+  if (n_rows * p.n_items <= 4096 && max_count >= 2 * kWarps) {
+    dim3 grid((unsigned)n_rows, p.n_items);
+    if (p.D == 128) {
+      mergen_split_kernel<128><<<grid, kWarps * 32, 0, stream>>>(p);
+    } else if (p.D == 64) {
+      mergen_split_kernel<64><<<grid, kWarps * 32, 0, stream>>>(p);
+    } else {
+      return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+  }
   const int64_t per_cta = (int64_t)kWarps * kRowsPerWarp;
   dim3 grid((unsigned)((n_rows + per_cta - 1) / per_cta), p.n_items);
   if (p.D == 128) {

@@ -62,6 +62,7 @@ def test_prefill_workload(B, name):
     (384, 768, 4, 1, 3, 384, "bf16"),       # more keys than queries, partial prefill
     (192, 192, 2, 1, 6, -64, "bf16"),       # first chunks see no key at all
     (240, 240, 2, 2, 5, 0, "fp32"),         # fp32 path, hq == hkv
+    (32, 4096, 2, 1, 32, 8192, "bf16"),     # one row per chunk, 32 partials per row
 ])
 def test_prefill_edge_cases(B, case, mode):
     sq, skv, hq, hkv, n, q_base, dt = case
