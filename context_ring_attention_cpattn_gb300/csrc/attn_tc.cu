@@ -59,7 +59,11 @@ struct Layout {
   static constexpr int kThreads = (4 * NT + 2) * 32;
   static constexpr int kTmaWarp = 4 * NT;
   static constexpr int kMmaWarp = 4 * NT + 1;
-  static constexpr int kTmemCols = NT == 2 ? 512 : 256;
+  // TMEM columns: NT == 2: S_0, S_1, O_0, O_1 (128 each).  NT == 1: S buffer
+  // 0, O, S buffer 1 (two score tiles, so the next QK product runs while the
+  // softmax works on the current one).
+  static constexpr int kTmemCols = 512;
+  static constexpr int kSBufs = NT == 1 ? 2 : 1;
   static constexpr int q_off = 0;
   static constexpr int k_off = q_off + NT * kTileBytes;
   static constexpr int v_off = k_off + kStages * kTileBytes;
@@ -71,11 +75,12 @@ struct Layout {
   static constexpr int b_kempty = b_kfull + kStages;
   static constexpr int b_vfull = b_kempty + kStages;
   static constexpr int b_vempty = b_vfull + kStages;
-  static constexpr int b_sfull = b_vempty + kStages;
-  static constexpr int b_pready = b_sfull + NT;
-  static constexpr int b_pvdone = b_pready + NT;
+  static constexpr int b_sfull = b_vempty + kStages;  // per tile, or per score buffer (NT == 1)
+  static constexpr int b_pready = b_sfull + NT * kSBufs;
+  static constexpr int b_pvdone = b_pready + NT * kSBufs;
   static constexpr int b_ofree = b_pvdone + NT;  // softmax warps have read O_t
-  static constexpr int b_drain = b_ofree + NT;
+  static constexpr int b_pvstep = b_ofree + NT;  // NT == 1: every PV MMA group done
+  static constexpr int b_drain = b_pvstep + 1;
   static constexpr int n_bars = b_drain + 1;
   static constexpr int tmem_slot_off = bar_off + n_bars * 8;
   static constexpr int abort_off = tmem_slot_off + 4;
@@ -271,12 +276,15 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
       mbar_init(bar(L::b_vfull + s), 1);
       mbar_init(bar(L::b_vempty + s), 1);
     }
-    for (int t = 0; t < NT; ++t) {
+    for (int t = 0; t < NT * L::kSBufs; ++t) {
       mbar_init(bar(L::b_sfull + t), 1);
       mbar_init(bar(L::b_pready + t), 4);
+    }
+    for (int t = 0; t < NT; ++t) {
       mbar_init(bar(L::b_pvdone + t), 1);
       mbar_init(bar(L::b_ofree + t), 4);
     }
+    mbar_init(bar(L::b_pvstep), 1);
     mbar_init(bar(L::b_drain), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -429,26 +437,87 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
       const uint64_t dk0 = make_sdesc(sb + L::k_off, 16, 1024);
       const uint64_t dv0 = make_sdesc(sb + L::v_off, kBoxBytes, 1024);
       constexpr uint64_t kTileStep = kTileBytes >> 4;
-      auto issue_qk = [&](int t, int st) {
+      // S (TMEM columns s_col..) = Q_t K^T; O (o_col..) (+)= P V with P in
+      // the first 64 columns of the score tile.
+      auto issue_qk_at = [&](int t, int st, int s_col) {
         const uint64_t dq = dq0 + (uint64_t)t * kTileStep;
         const uint64_t dk = dk0 + (uint64_t)st * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint64_t off = (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
-          mma_ss(tmem + t * 128, dq + off, dk + off, kIdescQK, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + s_col, dq + off, dk + off, kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int st, bool accumulate) {
+      auto issue_pv_at = [&](int s_col, int o_col, int st, bool accumulate) {
         const uint64_t dv = dv0 + (uint64_t)st * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          mma_ts(tmem + (NT + t) * 128, tmem + t * 128 + kk * 8,
+          mma_ts(tmem + o_col, tmem + s_col + kk * 8,
                  dv + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
         }
       };
+      auto issue_qk = [&](int t, int st) { issue_qk_at(t, st, t * 128); };
+      auto issue_pv = [&](int t, int st, bool accumulate) {
+        issue_pv_at(t * 128, (NT + t) * 128, st, accumulate);
+      };
       bool ok = true;
       int g = 0, nitem = 0;  // KV steps and non-empty items issued so far
-      for (int item = blockIdx.x; item < p.total_ctas && ok; item += stride) {
+      if constexpr (NT == 1) {
+        // One tile, two score buffers (step g uses buffer g & 1, at TMEM
+        // column 256 * (g & 1)); O at column 128.  QK of step g + 2 reuses
+        // the buffer whose P the PV of step g reads, and is issued right after
+        // it (in-order tensor pipe; kStrictOrder waits for every PV instead).
+        // Every PV commits pvstep: the softmax of step g + 1 may run before
+        // the PV of step g completes and must wait for it before rescaling O.
+        // (Phase-parity waits stay unambiguous: when the softmax of step g + 1
+        // waits, the PV of step g - 1 is complete -- the QK of step g + 1 was
+        // issued after it -- and the PV of step g + 1 cannot be.)  pvdone
+        // completes once per item, after its last PV.
+        auto qk_step = [&](int gk, bool last_qk) -> bool {
+          const int sk = gk % L::kStages;
+          if (!wait_bar(bar(L::b_kfull + sk), (gk / L::kStages) & 1, abort_flag)) return false;
+          tc_fence_after();
+          issue_qk_at(0, sk, (gk & 1) * 256);
+          mma_commit(bar(L::b_sfull + (gk & 1)));
+          mma_commit(bar(L::b_kempty + sk));
+          if (kPersistent && last_qk) mma_commit(bar(L::b_qempty));
+          return true;
+        };
+        for (int item = blockIdx.x; item < p.total_ctas && ok; item += stride) {
+          Item it;
+          decode(item, it);
+          const int n_kv = it.n_kv;
+          if (n_kv == 0) continue;
+          if (!wait_bar(bar(L::b_qfull), nitem & 1, abort_flag)) { ok = false; break; }
+          for (int j = 0; j < 2 && j < n_kv && ok; ++j) ok = qk_step(g + j, j == n_kv - 1);
+          for (int j = 0; j < n_kv && ok; ++j) {
+            const int gj = g + j;
+            const int buf = gj & 1;
+            const int sv = gj % L::kStages;
+            if (!wait_bar(bar(L::b_vfull + sv), (gj / L::kStages) & 1, abort_flag) ||
+                !wait_bar(bar(L::b_pready + buf), (gj >> 1) & 1, abort_flag) ||
+                (kPersistent && j == 0 && nitem > 0 &&
+                 !wait_bar(bar(L::b_ofree), (nitem - 1) & 1, abort_flag))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv_at(buf * 256, 128, sv, j > 0);
+            mma_commit(bar(L::b_vempty + sv));
+            mma_commit(bar(L::b_pvstep));
+            if (j == n_kv - 1) mma_commit(bar(L::b_pvdone));
+            if (kStrictOrder && !wait_bar(bar(L::b_pvstep), gj & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (j + 2 < n_kv) ok = qk_step(gj + 2, j + 2 == n_kv - 1);
+          }
+          g += n_kv;
+          ++nitem;
+          if constexpr (!kPersistent) break;
+        }
+      }
+      for (int item = blockIdx.x; item < p.total_ctas && ok && NT == 2; item += stride) {
         Item it;
         decode(item, it);
         const int n_kv = it.n_kv;
@@ -524,7 +593,7 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // row in the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + t * 128;
+    const uint32_t t_s0 = tmem + lane_off + t * 128;  // NT == 1: buffer 0; buffer 1 at + 256
     const uint32_t t_o = tmem + lane_off + (NT + t) * 128;
     const float sl2 = p.scale_log2;
     bool ok = true;
@@ -546,7 +615,11 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < n_kv; ++j) {
         // Warp-uniform outcome: the TMEM accesses below are warp-collective.
-        if (!__all_sync(0xffffffffu, wait_bar(bar(L::b_sfull + t), (g + j) & 1, abort_flag))) {
+        // Score buffer of this step and the phase of its barrier.
+        const int sbuf = NT == 1 ? ((g + j) & 1) : t;
+        const uint32_t sphase = NT == 1 ? (((g + j) >> 1) & 1) : ((g + j) & 1);
+        const uint32_t t_s = t_s0 + (NT == 1 ? (uint32_t)((g + j) & 1) * 256u : 0u);
+        if (!__all_sync(0xffffffffu, wait_bar(bar(L::b_sfull + sbuf), sphase, abort_flag))) {
           ok = false;
           break;
         }
@@ -585,6 +658,15 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
         const bool rescale_o = grow && (m_run != -INFINITY) && j > 0;
         if (grow) m_run = m_new;
         if (__any_sync(0xffffffffu, rescale_o)) {
+          if (NT == 1) {
+            // The previous step's PV may still be accumulating into O.
+            if (!__all_sync(0xffffffffu,
+                            wait_bar(bar(L::b_pvstep), (g + j - 1) & 1, abort_flag))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           const float a = rescale_o ? alpha : 1.f;
 #pragma unroll
           for (int cc = 0; cc < kD / 32; ++cc) {
@@ -623,14 +705,15 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::b_pready + t));
+        if (lane == 0) mbar_arrive(bar(L::b_pready + sbuf));
       }
       if (!ok) break;
 
       // ---- epilogue: O_t / l, LSE, routed by the pair's role
       if (n_kv > 0) {
-        // pvdone_t completes once per KV step in the strict schedule, else once per item.
-        const uint32_t par = kStrictOrder ? ((g + n_kv - 1) & 1) : (nitem & 1);
+        // pvdone_t completes once per KV step in the two-tile strict
+        // schedule, else once per item.
+        const uint32_t par = (kStrictOrder && NT == 2) ? ((g + n_kv - 1) & 1) : (nitem & 1);
         ok = __all_sync(0xffffffffu, wait_bar(bar(L::b_pvdone + t), par, abort_flag));
         tc_fence_after();
         if (!ok) break;

@@ -152,13 +152,16 @@ def test_argument_errors_do_not_launch(B):
     assert err.value.status == 2   # head_dim 96 unsupported
 
 
-@pytest.mark.parametrize("case", [TC_CASES[1], TC_CASES[2], TC_CASES[4], TC_CASES[5]],
+@pytest.mark.parametrize("case", [TC_CASES[1], TC_CASES[2], TC_CASES[3], TC_CASES[4], TC_CASES[5],
+                                  (300, 2000, 3, 3, 128, 1700, 0, True)],
                          ids=lambda c: "x".join(map(str, c)))
 def test_strict_mma_order_matches_default(B, case, monkeypatch):
-    """The default MMA schedule lets S_t(j+1) follow O_t += P_t(j) V_j without
-    waiting (it relies on the tensor pipe running one thread's MMAs in issue
-    order).  CPATTN_STRICT_MMA_ORDER=1 waits for each PV MMA instead.  Both
-    must give bitwise the same result, and both must match the oracle."""
+    """The default MMA schedule lets a QK product follow the PV MMA that reads
+    the same TMEM columns without waiting (it relies on the tensor pipe running
+    one thread's MMAs in issue order).  CPATTN_STRICT_MMA_ORDER=1 waits for
+    each PV MMA instead.  Both must give bitwise the same result, and both must
+    match the oracle.  Hq == Hkv cases run the one-tile kernel with two score
+    buffers."""
     sq, skv, hq, hkv, d, q_off, kv_off, causal = case
     q = rand((1, sq, hq, d), torch.bfloat16, 21)
     k = rand((1, skv, hkv, d), torch.bfloat16, 22)
