@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # DRAM bytes (read + write) per tensor FLOP of the tensor-core attention
 # kernel from one ncu capture, and the kernel source it was taken from; the
 # roofline's traffic is null whenever the source differs from the capture.
-TRAFFIC_RECORD = {"sha": "626b398f39eda971", "bytes_per_flop": 3.0386e-4,
+TRAFFIC_RECORD = {"sha": "51e15daff5bf4048", "bytes_per_flop": 3.0397e-4,
                   "capture": "profiles/attn_tc_128k_passkv_step2.md"}
 
 
@@ -317,12 +317,16 @@ def time_decode(B, steps, hbm_peak, peak_src, name="decode-128k-b8"):
     n = max(20, steps * 4)
     # Flush L2 between calls so each one streams the cache from HBM (K/V are
     # 512 MiB in total, larger than L2, but the tail of one call is still
-    # resident at the start of the next).
+    # resident at the start of the next): write 256 MiB, then read another
+    # 256 MiB so that the written lines are back in HBM before the timed call
+    # starts (their write-back would otherwise compete with the call).
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    clean = torch.ones(256 << 20, dtype=torch.uint8, device="cuda")
     B.profile_begin(4 * n)
     evs = []
     for _ in range(n):
         flush.zero_()
+        clean.max()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         run()
@@ -338,14 +342,14 @@ def time_decode(B, steps, hbm_peak, peak_src, name="decode-128k-b8"):
     total = kv_bytes + 2.0 * part_bytes + qo_bytes
     attn = [r for r in recs if r[0] == "attn_tc"]
     attn_ms = statistics.median(r[1] for r in attn) if attn else None
-    del q, k, v, out, ws, flush
+    del q, k, v, out, ws, flush, clean
     torch.cuda.empty_cache()
     return {"workload": name, "ms_per_call": ms, "tokens_per_s": w.batch * w.sq / (ms * 1e-3),
             "achieved": total / (ms * 1e-3) / 1e9, "unit": "GB/s", "peak": hbm_peak,
             "frac": total / (ms * 1e-3) / 1e9 / hbm_peak, "bytes_per_call": total,
             "attn_kernel": {"ms": attn_ms, "kv_GBs": (kv_bytes / (attn_ms * 1e-3) / 1e9) if attn_ms else None,
                             "frac": (kv_bytes / (attn_ms * 1e-3) / 1e9 / hbm_peak) if attn_ms else None},
-            "l2": "256 MiB written between calls (L2 flush)", "peak_source": f"{peak_src} HBM copy"}
+            "l2": "256 MiB written, then 256 MiB read, between calls (L2 flush)", "peak_source": f"{peak_src} HBM copy"}
 
 
 def make_buffers(B, w, q, k, modes, launch=0):
