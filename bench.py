@@ -485,6 +485,21 @@ def main():
                               "pass_q_ring_bytes": qb}
     if len(modes) == 2:
         cfg["schedule_choice"]["faster_on_one_gpu"] = min(ms_layer, key=ms_layer.get)
+        # Partial prefill (2048 new tokens against a 32768-token cache), where
+        # the schedules move different amounts: the model's pick and both
+        # schedules timed (ms per layer, median).
+        wp = WORKLOADS["partial-32k"]
+        qp, kp, vp = make_qkv(wp, device="cuda")
+        outsp, wssp = make_buffers(B, wp, qp, kp, modes, launch)
+        _, pmp, _ = time_modes(B, wp, qp, kp, vp, outsp, wssp, max(10, args.steps), args.warmup,
+                               world, modes, launch=launch)
+        mode_p, kvp, qbp = B.choose_mode(qp, kp, wp.n_chunks)
+        msp = {names[m]: statistics.median(pmp[m]) for m in modes}
+        cfg["schedule_choice_partial_32k"] = {"model_picks": names[mode_p],
+                                              "pass_kv_ring_bytes": kvp, "pass_q_ring_bytes": qbp,
+                                              "ms_per_layer": msp,
+                                              "faster_on_one_gpu": min(msp, key=msp.get)}
+        del qp, kp, vp, outsp, wssp
 
     # ---- 1M-token layer (ms/layer only)
     if not args.skip_1m and w.name != "1m":

@@ -176,3 +176,26 @@ def test_single_launch_wait_runs_out(B):
     torch.cuda.synchronize()
     assert B.device_status() == 0
     assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("assignment", [0, 1])
+def test_prefill_batch_strides_and_mask(B, mode, causal, assignment):
+    """Batch 2, a Q that is a head-dim slice of a wider buffer (row and head
+    strides of the view, not of a dense tensor), with and without the causal
+    mask, both chunk assignments: every row against the oracle."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4242 + mode)
+    base = torch.randn((2, 1024, 8, 256), generator=g, device="cuda").to(torch.bfloat16)
+    q = base[..., 128:]
+    k = torch.randn((2, 1024, 2, 128), generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn((2, 1024, 2, 128), generator=g, device="cuda").to(torch.bfloat16)
+    o, lse = B.prefill(q, k, v, 4, mode, causal=causal, assignment=assignment)
+    torch.cuda.synchronize()
+    assert B.device_status() == 0
+    rows = np.arange(1024)
+    for b in range(2):
+        ref_o, ref_l = oracle_rows(q[b:b + 1], k[b:b + 1], v[b:b + 1], rows, causal=causal)
+        compare(o[b:b + 1], lse[b:b + 1], rows, ref_o, ref_l, TOL["bf16"],
+                f"batch {b} mode {mode} causal {causal} assignment {assignment}")
