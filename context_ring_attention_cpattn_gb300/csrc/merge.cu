@@ -25,7 +25,7 @@ namespace cpattn {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kRowsPerWarp = 2;  // rows per warp, loads of all of them in flight together
+constexpr int kRowsPerWarp = 2;  // pairwise merge: rows per warp, all their loads in flight together
 
 template <int E>
 __device__ __forceinline__ void load_row(const OutView &w, int b, int64_t row, int h, int c0,
@@ -77,26 +77,26 @@ __global__ void __launch_bounds__(kWarps * 32) merge2_kernel(const __grid_consta
 
 // Pass-Q: for item x, rows [0, chunk_rows) of Q chunk x merge slots
 // slot0 .. slot0 + count - 1 (ascending KV chunk) into the final output.
-// One pass with a running maximum: every group of kInFlight partials (their
-// LSE and O rows, for kRowsPerWarp rows at once) is loaded before any of it
-// is used, so each warp keeps up to kRowsPerWarp * kInFlight 512-byte rows in
+// One pass with a running maximum: every group of F partials (their LSE and O
+// rows, for R rows at once) is loaded before any of it is used, so each warp
+// keeps up to R * F 512-byte rows in
 // flight and pays one memory round trip per group.
-template <int D>
+template <int D, int R, int F>
 __global__ void __launch_bounds__(kWarps * 32) mergen_kernel(const __grid_constant__ MergeNParams p) {
   constexpr int E = D / 32;
-  constexpr int kInFlight = 8;
+  constexpr int kInFlight = F;
   const int lane = threadIdx.x & 31;
   const int item = blockIdx.y;
   const int count = p.item_count[item];
   const int slot0 = p.item_slot0[item];
   const int64_t n_rows = (int64_t)p.B * p.chunk_rows * p.H;
-  const int64_t r0 = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRowsPerWarp;
+  const int64_t r0 = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * R;
   if (r0 >= n_rows) return;
-  const float *lse0[kRowsPerWarp];
-  const float *o0[kRowsPerWarp];
-  float m[kRowsPerWarp], sum[kRowsPerWarp], acc[kRowsPerWarp][E];
+  const float *lse0[R];
+  const float *o0[R];
+  float m[R], sum[R], acc[R][E];
 #pragma unroll
-  for (int u = 0; u < kRowsPerWarp; ++u) {
+  for (int u = 0; u < R; ++u) {
     const int64_t r = r0 + u < n_rows ? r0 + u : r0;  // a duplicate row is computed, not stored
     const int h = (int)(r % p.H);
     const int64_t s = (r / p.H) % p.chunk_rows;
@@ -111,10 +111,10 @@ __global__ void __launch_bounds__(kWarps * 32) mergen_kernel(const __grid_consta
     for (int i = 0; i < E; ++i) acc[u][i] = 0.f;
   }
   for (int j0 = 0; j0 < count; j0 += kInFlight) {
-    float l[kRowsPerWarp][kInFlight];
-    float v[kRowsPerWarp][kInFlight][E];
+    float l[R][kInFlight];
+    float v[R][kInFlight][E];
 #pragma unroll
-    for (int u = 0; u < kRowsPerWarp; ++u)
+    for (int u = 0; u < R; ++u)
 #pragma unroll
       for (int x = 0; x < kInFlight; ++x) {
         if (j0 + x < count) {
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kWarps * 32) mergen_kernel(const __grid_consta
         }
       }
 #pragma unroll
-    for (int u = 0; u < kRowsPerWarp; ++u) {
+    for (int u = 0; u < R; ++u) {
       float mg = l[u][0];
 #pragma unroll
       for (int x = 1; x < kInFlight; ++x) mg = fmaxf(mg, l[u][x]);
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kWarps * 32) mergen_kernel(const __grid_consta
     }
   }
 #pragma unroll
-  for (int u = 0; u < kRowsPerWarp; ++u) {
+  for (int u = 0; u < R; ++u) {
     const int64_t r = r0 + u;
     if (r >= n_rows) break;
     const int h = (int)(r % p.H);
@@ -295,12 +295,16 @@ cudaError_t launch_merge_n(const MergeNParams &p, cudaStream_t stream) {
     }
     return cudaGetLastError();
   }
-  const int64_t per_cta = (int64_t)kWarps * kRowsPerWarp;
+  // Two rows per warp, two partials of each in flight: few registers, so many
+  // warps per SM keep the loads in flight.  Measured at the 128K Pass-Q shape
+  // (GB/s): 2 x 2 5880, 2 x 4 5620, 1 x 3 5770, 4 x 4 5060, 2 x 8 4220.
+  constexpr int kR = 2, kF = 2;
+  const int64_t per_cta = (int64_t)kWarps * kR;
   dim3 grid((unsigned)((n_rows + per_cta - 1) / per_cta), p.n_items);
   if (p.D == 128) {
-    mergen_kernel<128><<<grid, kWarps * 32, 0, stream>>>(p);
+    mergen_kernel<128, kR, kF><<<grid, kWarps * 32, 0, stream>>>(p);
   } else if (p.D == 64) {
-    mergen_kernel<64><<<grid, kWarps * 32, 0, stream>>>(p);
+    mergen_kernel<64, kR, kF><<<grid, kWarps * 32, 0, stream>>>(p);
   } else {
     return cudaErrorInvalidValue;
   }
