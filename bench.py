@@ -375,7 +375,8 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-decode", action="store_true", help="do not time the decode leg")
     ap.add_argument("--launch", type=int, default=None,
-                    help="ring launch mode: 0 per step, 1 persistent per step, 2 one launch")
+                    help="ring launch mode: 0 per step, 1 persistent per step, 2 one launch, "
+                         "3 auto (the library default)")
     ap.add_argument("--schedules", default="both", choices=["both", "kv", "q"],
                     help="ring schedules in one step (default: Pass-KV then Pass-Q)")
     ap.add_argument("--cpu-rows", type=int, default=2048,
@@ -406,7 +407,7 @@ def main():
 
     modes = {"both": (B.PASS_KV, B.PASS_Q), "kv": (B.PASS_KV,), "q": (B.PASS_Q,)}[args.schedules]
     names = {B.PASS_KV: "pass_kv", B.PASS_Q: "pass_q"}
-    launch = B.LAUNCH_PER_STEP if args.launch is None else args.launch
+    launch = B.LAUNCH_AUTO if args.launch is None else args.launch
     q, k, v = make_qkv(w, device="cuda")
     outs, wss = make_buffers(B, w, q, k, modes, launch)
     flops_layer = w.causal_flops()
@@ -470,8 +471,11 @@ def main():
     decode = None if args.skip_decode else time_decode(B, args.steps, hbm_peak, peak_src)
     cfg = {"workload": w.name, "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim,
            "seq_len": w.sq, "n_chunks": w.n_chunks, "causal": w.causal,
-           "launch_mode": ["one launch per ring step", "persistent CTAs per ring step",
-                           "one persistent launch for all ring steps"][launch],
+           "launch_mode": ("auto: " if launch == B.LAUNCH_AUTO else "") +
+                          ["one launch per ring step", "persistent CTAs per ring step",
+                           "one persistent launch for all ring steps"][
+                              B.launch_mode(q, k, w.n_chunks, modes[0], w.q_base, w.causal,
+                                            launch=launch)],
            "step": " + ".join({"pass_kv": "Pass-KV prefill", "pass_q": "Pass-Q prefill"}[names[m]]
                                for m in modes) + " of one layer",
            "flops_per_layer": flops_layer, "ms_per_layer": ms_layer,

@@ -38,10 +38,10 @@ class PrefillOptions(ctypes.Structure):
 
 
 ASSIGN_CONTIGUOUS, ASSIGN_ZIGZAG = 0, 1
-LAUNCH_PER_STEP, LAUNCH_PERSISTENT_STEP, LAUNCH_SINGLE = 0, 1, 2
+LAUNCH_PER_STEP, LAUNCH_PERSISTENT_STEP, LAUNCH_SINGLE, LAUNCH_AUTO = 0, 1, 2, 3
 
 
-def _opts(assignment: int, launch: int = LAUNCH_PER_STEP, hold_ordered_waits: bool = False):
+def _opts(assignment: int, launch: int = LAUNCH_AUTO, hold_ordered_waits: bool = False):
     return ctypes.byref(PrefillOptions(int(assignment), int(launch), int(bool(hold_ordered_waits))))
 
 
@@ -50,6 +50,7 @@ class ProfileRecord(ctypes.Structure):
 
 
 EXPORTED = ["cpattn_partial", "cpattn_merge", "cpattn_prefill_workspace_size", "cpattn_prefill",
+            "cpattn_prefill_launch_mode",
             "cpattn_prefill_plan", "cpattn_prefill_host_scratch_size", "cpattn_prefill_host",
             "cpattn_prefill_noalloc", "cpattn_decode_workspace_size", "cpattn_decode",
             "cpattn_prefill_ex", "cpattn_prefill_workspace_size_ex", "cpattn_prefill_plan_ex",
@@ -103,6 +104,8 @@ def lib():
                                          i32, ctypes.POINTER(ctypes.c_int)]
     L.cpattn_prefill_critical_path.argtypes = [i64, i64, i64, i32, i32, i32, O, dp, dp, dp]
     L.cpattn_prefill_choose_mode.argtypes = [T, T, i32, ctypes.POINTER(ctypes.c_int), dp, dp]
+    L.cpattn_prefill_launch_mode.argtypes = [T, T, i64, i32, i32, i32, O,
+                                             ctypes.POINTER(ctypes.c_int)]
     L.cpattn_decode.argtypes = [T, T, T, i64, i32, i32, f32, T, vp, vp, ctypes.c_size_t, vp]
     L.cpattn_status_string.argtypes = [i32]
     L.cpattn_status_string.restype = ctypes.c_char_p
@@ -176,7 +179,7 @@ def merge_(o_a, lse_a, o_b, lse_b, stream=None):
 
 
 def workspace_size(q, k, n_chunks: int, mode: int, q_base: int = 0, causal: bool = True,
-                   assignment: int = ASSIGN_CONTIGUOUS, launch: int = LAUNCH_PER_STEP) -> int:
+                   assignment: int = ASSIGN_CONTIGUOUS, launch: int = LAUNCH_AUTO) -> int:
     n = ctypes.c_size_t(0)
     qv, kv_ = view(q), view(k)
     _check(lib().cpattn_prefill_workspace_size_ex(ctypes.byref(qv), ctypes.byref(kv_), int(q_base),
@@ -188,7 +191,7 @@ def workspace_size(q, k, n_chunks: int, mode: int, q_base: int = 0, causal: bool
 
 def prefill(q, k, v, n_chunks: int, mode: int, q_base: int = 0, causal: bool = True, scale=None,
             out=None, lse=None, workspace=None, out_dtype=None, stream=None,
-            assignment: int = ASSIGN_CONTIGUOUS, launch: int = LAUNCH_PER_STEP,
+            assignment: int = ASSIGN_CONTIGUOUS, launch: int = LAUNCH_AUTO,
             hold_ordered_waits: bool = False):
     """CP prefill of one attention layer on one GPU; see cpattn_prefill_ex.
     ``hold_ordered_waits`` exists only to test failure detection."""
@@ -305,6 +308,18 @@ def prefill_plan(sq: int, skv: int, n_chunks: int, mode: int, q_base: int = 0,
         return [(e.step, e.q_chunk, e.kv_chunk, e.role, e.slot, e.launch, e.rank)
                 for e in arr[:n.value]]
     return [(e.step, e.q_chunk, e.kv_chunk, e.role, e.slot) for e in arr[:n.value]]
+
+
+def launch_mode(q, k, n_chunks: int, mode: int, q_base: int = 0, causal: bool = True,
+                assignment: int = ASSIGN_CONTIGUOUS, launch: int = LAUNCH_AUTO) -> int:
+    """The launch mode cpattn_prefill_ex uses for these shapes (AUTO resolved)."""
+    out = ctypes.c_int(0)
+    qv, kv_ = view(q), view(k)
+    _check(lib().cpattn_prefill_launch_mode(ctypes.byref(qv), ctypes.byref(kv_), int(q_base),
+                                            int(n_chunks), int(mode), int(bool(causal)),
+                                            _opts(assignment, launch), ctypes.byref(out)),
+           "cpattn_prefill_launch_mode")
+    return out.value
 
 
 def choose_mode(q, k, n_chunks: int):

@@ -221,13 +221,20 @@ typedef enum { CPATTN_ASSIGN_CONTIGUOUS = 0, CPATTN_ASSIGN_ZIGZAG = 1 } cpattn_a
  *                        waits -- bounded, CPATTN_ERR_TIMEOUT if it gives up --
  *                        until the previous step's update of the same rows has
  *                        finished.  Launched cooperatively (all CTAs resident).
- * CPATTN_LAUNCH_DEFAULT is PER_STEP.
+ *   AUTO                 SINGLE when the tensor-core kernel applies (bf16,
+ *                        head_dim 128) and the ring's work items are short --
+ *                        fewer than 48 visible 128-key tiles per 128-row
+ *                        query tile on average, where a CTA's fixed start-up
+ *                        and write-out cost is a large share of its work --
+ *                        else PER_STEP.
+ * CPATTN_LAUNCH_DEFAULT (options NULL or launch = DEFAULT) is AUTO.
  */
 typedef enum {
   CPATTN_LAUNCH_PER_STEP = 0,
   CPATTN_LAUNCH_PERSISTENT_STEP = 1,
   CPATTN_LAUNCH_SINGLE = 2,
-  CPATTN_LAUNCH_DEFAULT = 0
+  CPATTN_LAUNCH_AUTO = 3,
+  CPATTN_LAUNCH_DEFAULT = 3
 } cpattn_launch_mode;
 
 /*
@@ -244,6 +251,15 @@ typedef struct {
   int32_t hold_ordered_waits;  /* see above; 0 */
   int32_t reserved[5];         /* zero */
 } cpattn_prefill_options;
+
+/*
+ * cpattn_prefill_launch_mode -- the launch mode cpattn_prefill_ex would use
+ * for these shapes and options (CPATTN_LAUNCH_AUTO resolved to PER_STEP or
+ * SINGLE; an explicit mode is returned as given).  Host only, no CUDA call.
+ */
+cpattn_status cpattn_prefill_launch_mode(const cpattn_tensor *q, const cpattn_tensor *k,
+                                         int64_t q_base, int n_chunks, int mode, int causal,
+                                         const cpattn_prefill_options *opts, int *launch);
 
 /* cpattn_prefill / _workspace_size / _plan with options (NULL = defaults). */
 cpattn_status cpattn_prefill_ex(const cpattn_tensor *q, const cpattn_tensor *k,

@@ -118,10 +118,13 @@ def test_prefill_argument_errors(lib):
     for n, mode in ((3, 1), (0, 1), (65, 1), (4, 3)):
         assert lib.cpattn_prefill_workspace_size(ctypes.byref(q), ctypes.byref(k), 0, n, mode, 1,
                                                  ctypes.byref(size)) == INVALID
+    per_step = ctypes.byref(B.PrefillOptions(0, B.LAUNCH_PER_STEP))
+    assert lib.cpattn_prefill_workspace_size_ex(ctypes.byref(q), ctypes.byref(k), 0, 4, 1, 1,
+                                                per_step, ctypes.byref(size)) == 0
+    assert size.value == 1024 * 8 * 128 * 4 + 1024 * 8 * 4   # the fp32 accumulator and its LSE
     assert lib.cpattn_prefill_workspace_size(ctypes.byref(q), ctypes.byref(k), 0, 4, 1, 1,
                                              ctypes.byref(size)) == 0
-    need = size.value
-    assert need == 1024 * 8 * 128 * 4 + 1024 * 8 * 4
+    need = size.value  # the default (AUTO) adds the single launch's pair table and counters
     # Missing / short / misaligned workspace is rejected before any launch.
     args = lambda ws, n: (ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), 0, 4, 1, 1, 0.0,
                           ctypes.byref(o), 0x20000, ws, n, None)
@@ -134,12 +137,44 @@ def test_workspace_sizes(lib):
     # Pass-Q keeps one fp32 partial per visible pair of chunks reached more than once.
     q, k = T(h=16, s=4096), T(h=1, s=4096)
     size = ctypes.c_size_t()
-    assert lib.cpattn_prefill_workspace_size(ctypes.byref(q), ctypes.byref(k), 0, 4, 2, 1,
-                                             ctypes.byref(size)) == 0
+    per_step = ctypes.byref(B.PrefillOptions(0, B.LAUNCH_PER_STEP))
+    assert lib.cpattn_prefill_workspace_size_ex(ctypes.byref(q), ctypes.byref(k), 0, 4, 2, 1,
+                                                per_step, ctypes.byref(size)) == 0
     slots = 2 + 3 + 4   # chunks 1..3 reach 2, 3, 4 KV chunks; chunk 0 reaches one
     per_slot_o, per_slot_l = 1024 * 16 * 128 * 4, 16 * 1024 * 4
     align = lambda x: (x + 255) // 256 * 256
     assert size.value == align(slots * per_slot_o) + align(slots * per_slot_l)
+
+
+@pytest.mark.parametrize("shape,dtype,want", [
+    ((8192, 8192, 32, 8, 8), B.BF16, B.LAUNCH_SINGLE),        # 8-tile work items
+    ((2048, 32768, 16, 1, 8), B.BF16, B.LAUNCH_SINGLE),       # partial prefill, 32-tile items
+    ((131072, 131072, 16, 1, 16), B.BF16, B.LAUNCH_PER_STEP),  # ~60-tile items
+    ((8192, 8192, 32, 8, 8), B.FP32, B.LAUNCH_PER_STEP),      # no tensor-core kernel
+])
+def test_auto_launch_mode(lib, shape, dtype, want):
+    """CPATTN_LAUNCH_AUTO (the default) resolves to one launch for all ring
+    steps when work items are short, one launch per step otherwise; the
+    default workspace size is the resolved mode's."""
+    sq, skv, hq, hkv, n = shape
+    q_base = skv - sq
+    q, k = T(dtype=dtype, s=sq, h=hq), T(dtype=dtype, s=skv, h=hkv)
+    got = ctypes.c_int(-1)
+    assert lib.cpattn_prefill_launch_mode(ctypes.byref(q), ctypes.byref(k), q_base, n, 1, 1, None,
+                                          ctypes.byref(got)) == 0
+    assert got.value == want
+    explicit = ctypes.byref(B.PrefillOptions(0, B.LAUNCH_PERSISTENT_STEP))
+    assert lib.cpattn_prefill_launch_mode(ctypes.byref(q), ctypes.byref(k), q_base, n, 1, 1, explicit,
+                                          ctypes.byref(got)) == 0
+    assert got.value == B.LAUNCH_PERSISTENT_STEP
+    for mode in (1, 2):
+        a, b = ctypes.c_size_t(), ctypes.c_size_t()
+        assert lib.cpattn_prefill_workspace_size(ctypes.byref(q), ctypes.byref(k), q_base, n, mode, 1,
+                                                 ctypes.byref(a)) == 0
+        resolved = ctypes.byref(B.PrefillOptions(0, want))
+        assert lib.cpattn_prefill_workspace_size_ex(ctypes.byref(q), ctypes.byref(k), q_base, n,
+                                                    mode, 1, resolved, ctypes.byref(b)) == 0
+        assert a.value == b.value
 
 
 def test_status_strings(lib):
