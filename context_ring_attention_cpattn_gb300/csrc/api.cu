@@ -305,7 +305,9 @@ struct WsLayout {
   size_t total = 0;
 };
 
-int64_t tiles_per_piece(const Plan &pl) { return (pl.Cq + 127) / 128; }
+// 128-row query tiles of a Q piece, rounded up to whole 256-row pairs (the
+// row-pair work items of odd GQA groups index their tiles up to there).
+int64_t tiles_per_piece(const Plan &pl) { return 2 * ((pl.Cq + 255) / 256); }
 
 WsLayout ws_layout(const Plan &pl, int64_t B, int64_t sq, int64_t hq, int64_t d,
                    int launch_mode = CPATTN_LAUNCH_PER_STEP) {
@@ -476,14 +478,14 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
       launch_items(e0, e1, table);
       e0 = e1;
     }
-    const int nt = attn_tc_tiles_per_cta(p);
+    const TcItemShape sh = attn_tc_item_shape(p);
     std::vector<int> visits(pl.P, 0);
     int total = 0;
     double vis = 0.0;
     for (auto &pd : table) {
-      pd.n_qtiles = (pd.q_len + 127) / 128;
+      pd.n_qtiles = (pd.q_len + sh.rows - 1) / sh.rows;
       pd.cta_begin = total;
-      total += pd.n_qtiles * (int)(q->h / nt) * (int)q->b;
+      total += pd.n_qtiles * (int)(q->h / sh.heads) * (int)q->b;
       const int piece = (int)(pd.q_row0 / pl.Cq);
       if (pd.mode == kAccInit || pd.mode == kAccMerge || pd.mode == kAccFinal)
         pd.visit = visits[piece]++;

@@ -244,7 +244,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // 4 KB kernel-parameter space.
 static_assert(sizeof(AttnParams) + 3 * sizeof(CUtensorMap) <= 4096, "kernel parameters too large");
 
-template <int NT, bool kStrictOrder, bool kPersistent>
+template <int NT, bool kStrictOrder, bool kPersistent, bool kRowPair>
 __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnParams p) {
@@ -260,6 +260,8 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
   const PairDesc *pairs = p.pair_table != nullptr ? p.pair_table : p.pairs;
   const int n_pairs = p.pair_table != nullptr ? p.n_table : p.n_pairs;
   const int G = NT == 1 ? p.pack_g : 0;  // query heads per tile in packed mode, else 0
+  static_assert(!kRowPair || NT == 2, "row pairs need two tiles per CTA");
+  constexpr bool RP = kRowPair;  // tiles = two row blocks of one head
   // Work items handled by this CTA: blockIdx.x, + stride, ... (one item when
   // the grid has a CTA per item; a loop in a persistent launch).
   // A non-persistent launch runs exactly one item per CTA, which the compiler
@@ -325,14 +327,17 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
     it.ks = 0;
     it.ke = pd.kv_len;
     if (G == 0) {
-      const int n_hg = p.Hq / NT;
+      // Tile t of the item: head h0 + t (two heads of a group) or, with row
+      // pairs, rows 128 t .. of the item's 256 rows of head h0.
+      const int hpi = RP ? 1 : NT, rpi = RP ? 2 * kBM : kBM;
+      const int n_hg = p.Hq / hpi;
       const int hg = local % n_hg;
       local /= n_hg;
       it.qt = pd.n_qtiles - 1 - local / p.B;  // longest tiles first
-      it.h0 = hg * NT;
+      it.h0 = hg * hpi;
       it.hk = it.h0 / (p.Hq / p.Hkv);
-      it.i0 = it.qt * kBM;
-      it.q_rows = min(kBM, pd.q_len - it.i0);
+      it.i0 = it.qt * rpi;
+      it.q_rows = min(rpi, pd.q_len - it.i0);
     } else {
       it.hk = local % p.Hkv;
       local /= p.Hkv;
@@ -376,7 +381,8 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
         for (int t = 0; t < NT; ++t)
           for (int half = 0; half < 2; ++half)
             tma_load_4d(sb + L::q_off + t * kTileBytes + half * kBoxBytes, &tm_q, bar(L::b_qfull),
-                        half * 64, it.h0 + t, it.pd->q_row0 + it.i0, it.b);  // packed map: heads h0..
+                        half * 64, it.h0 + (RP ? 0 : t), it.pd->q_row0 + it.i0 + (RP ? t * kBM : 0),
+                        it.b);  // packed map: heads h0..
         ++issued_q;
         for (int j = 0; j < it.n_kv; ++j, ++g) {
           const int st = g % L::kStages;
@@ -604,9 +610,10 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
       const PairDesc &pd = *it.pd;
       const int n_kv = it.n_kv;
       // Query row (inside the pair's chunk) and head of this tile row.
-      const int qrow = G == 0 ? it.i0 + r : r / G;
-      const int head = G == 0 ? it.h0 + t : it.h0 + r % G;
-      const bool valid = G == 0 ? r < it.q_rows : qrow < it.q_rows;
+      const int trow = RP ? t * kBM + r : r;  // row within the item
+      const int qrow = G == 0 ? it.i0 + trow : r / G;
+      const int head = G == 0 ? it.h0 + (RP ? 0 : t) : it.h0 + r % G;
+      const bool valid = G == 0 ? trow < it.q_rows : qrow < it.q_rows;
       int64_t lim = it.ke;  // this row's visible keys: [ks, lim)
       if (p.causal) {
         const int64_t c = (int64_t)qrow + pd.delta + 1;
@@ -738,7 +745,8 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
       int32_t *dep = nullptr;
       if (kPersistent && p.dep_counters != nullptr && G == 0 &&
           (pd.mode == kAccInit || pd.mode == kAccMerge || pd.mode == kAccFinal))
-        dep = p.dep_counters + pd.dep_base + ((int64_t)it.qt * p.Hq + head) * p.B + it.b;
+        dep = p.dep_counters + pd.dep_base +
+              ((int64_t)(RP ? it.qt * 2 + t : it.qt) * p.Hq + head) * p.B + it.b;
       // Each of the tile's 4 warps adds 1 when its rows are written, so the
       // rows' earlier visits are done once the count reaches 4 * visit.  Every
       // warp waits and publishes for itself: no barrier spans warps whose
@@ -844,7 +852,7 @@ bool make_map(CUtensorMap *map, const void *base, int64_t B, int64_t S, int64_t 
   return r == CUDA_SUCCESS;
 }
 
-template <int NT, bool kStrictOrder, bool kPersistent>
+template <int NT, bool kStrictOrder, bool kPersistent, bool kRowPair>
 cudaError_t launch_nt(AttnParams &p, cudaStream_t stream) {
   using L = Layout<NT>;
   int total = 0;
@@ -859,9 +867,10 @@ cudaError_t launch_nt(AttnParams &p, cudaStream_t stream) {
       pd.cta_begin = total;
       total += pd.n_qtiles * p.Hkv * p.B;
     } else {
-      pd.n_qtiles = (pd.q_len + kBM - 1) / kBM;
+      const TcItemShape sh = attn_tc_item_shape(p);
+      pd.n_qtiles = (pd.q_len + sh.rows - 1) / sh.rows;
       pd.cta_begin = total;
-      total += pd.n_qtiles * (p.Hq / NT) * p.B;
+      total += pd.n_qtiles * (p.Hq / sh.heads) * p.B;
     }
   }
   if (p.pair_table == nullptr) p.total_ctas = total;
@@ -878,7 +887,7 @@ cudaError_t launch_nt(AttnParams &p, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NT, kStrictOrder, kPersistent>,
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NT, kStrictOrder, kPersistent, kRowPair>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::alloc_bytes);
     if (e != cudaSuccess) return e;
@@ -906,7 +915,8 @@ cudaError_t launch_nt(AttnParams &p, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<NT, kStrictOrder, kPersistent>, mq, mk, mv, p);
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<NT, kStrictOrder, kPersistent, kRowPair>, mq, mk,
+                            mv, p);
 }
 
 }  // namespace
@@ -931,21 +941,29 @@ bool strict_mma_order() {
   return e != nullptr && e[0] != '\0' && e[0] != '0';
 }
 
-int attn_tc_tiles_per_cta(const AttnParams &p) {
-  return (p.pack_g == 0 && (p.Hq / p.Hkv) % 2 == 0) ? 2 : 1;
+TcItemShape attn_tc_item_shape(const AttnParams &p) {
+  if (p.pack_g > 0) return {kBM, 1};
+  return (p.Hq / p.Hkv) % 2 == 0 ? TcItemShape{kBM, 2} : TcItemShape{2 * kBM, 1};
 }
 
-template <int NT>
+template <int NT, bool kRowPair>
 cudaError_t launch_nt_any(AttnParams &p, cudaStream_t stream, bool strict) {
   const bool pers = p.persistent_ctas > 0;
-  if (strict) return pers ? launch_nt<NT, true, true>(p, stream) : launch_nt<NT, true, false>(p, stream);
-  return pers ? launch_nt<NT, false, true>(p, stream) : launch_nt<NT, false, false>(p, stream);
+  if (strict)
+    return pers ? launch_nt<NT, true, true, kRowPair>(p, stream)
+                : launch_nt<NT, true, false, kRowPair>(p, stream);
+  return pers ? launch_nt<NT, false, true, kRowPair>(p, stream)
+              : launch_nt<NT, false, false, kRowPair>(p, stream);
 }
 
 cudaError_t launch_attn_tc(AttnParams &p, cudaStream_t stream) {
   const bool strict = strict_mma_order();
-  if (attn_tc_tiles_per_cta(p) == 2) return launch_nt_any<2>(p, stream, strict);
-  return launch_nt_any<1>(p, stream, strict);
+  // Per-head tiles always pair two 128-row tiles in a CTA (two heads of a
+  // group, or two row blocks of one head); packed decode tiles run alone.
+  p.row_pair = (p.pack_g == 0 && (p.Hq / p.Hkv) % 2 != 0) ? 1 : 0;
+  if (p.pack_g != 0) return launch_nt_any<1, false>(p, stream, strict);
+  return p.row_pair ? launch_nt_any<2, true>(p, stream, strict)
+                    : launch_nt_any<2, false>(p, stream, strict);
 }
 
 unsigned int attn_tc_read_status(bool clear, cudaError_t *err) {

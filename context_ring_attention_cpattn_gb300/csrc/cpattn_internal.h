@@ -62,6 +62,10 @@ struct AttnParams {
   // and each CTA takes kv_split keys of its pair, writing an fp32 partial to
   // slot pairs[x].slot + split.  pack_g = 0: one head per tile row block.
   int32_t pack_g;
+  // Per-head tiles (pack_g == 0) with an odd group size Hq / Hkv: a work item
+  // is two consecutive 128-row query tiles of one head (which share every K/V
+  // tile) instead of one 128-row tile of two heads (filled by the launcher).
+  int32_t row_pair;
   int32_t kv_split;
   // Work items: pairs[] (at most kMaxPairs) or, when pair_table is set, a
   // device-resident table of n_table pairs (all ring steps of one call).
@@ -113,8 +117,13 @@ cudaError_t launch_merge_2(const Merge2Params &p, cudaStream_t stream);
 
 // True when the tensor-core kernel supports these shapes.
 bool attn_tc_supported(const AttnParams &p);
-// Query tiles (heads) per CTA the tensor-core kernel uses for these shapes.
-int attn_tc_tiles_per_cta(const AttnParams &p);
+// Per-head work items of the tensor-core kernel (pack_g == 0): query rows
+// and heads per item -- 128 rows of 2 heads sharing a kv head when Hq / Hkv
+// is even, else 256 rows (two 128-row tiles) of 1 head.
+struct TcItemShape {
+  int rows, heads;
+};
+TcItemShape attn_tc_item_shape(const AttnParams &p);
 
 // Device status words (one per translation unit that has bounded waits).
 unsigned int attn_tc_read_status(bool clear, cudaError_t *err);

@@ -35,6 +35,8 @@ TC_CASES = [
     (130, 1000, 2, 1, 128, 20, 900, True),      # most rows empty (keys in the future)
     (1, 1, 2, 1, 128, 0, 0, True),              # single row and key
     (64, 0, 2, 1, 128, 0, 0, True),             # no keys at all
+    (700, 700, 3, 3, 128, 0, 0, True),          # MHA: two row blocks of one head per CTA
+    (300, 500, 6, 2, 128, 100, 0, True),        # odd group size 3, ragged row pair
 ]
 
 

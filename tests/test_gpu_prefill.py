@@ -63,6 +63,8 @@ def test_prefill_workload(B, name):
     (192, 192, 2, 1, 6, -64, "bf16"),       # first chunks see no key at all
     (240, 240, 2, 2, 5, 0, "fp32"),         # fp32 path, hq == hkv
     (32, 4096, 2, 1, 32, 8192, "bf16"),     # one row per chunk, 32 partials per row
+    (640, 640, 3, 3, 5, 0, "bf16"),         # MHA, 128-row chunks (second row block empty)
+    (1000, 1000, 6, 2, 8, 0, "bf16"),       # odd group size 3, ragged row pairs
 ])
 def test_prefill_edge_cases(B, case, mode):
     sq, skv, hq, hkv, n, q_base, dt = case
@@ -199,3 +201,29 @@ def test_prefill_batch_strides_and_mask(B, mode, causal, assignment):
         ref_o, ref_l = oracle_rows(q[b:b + 1], k[b:b + 1], v[b:b + 1], rows, causal=causal)
         compare(o[b:b + 1], lse[b:b + 1], rows, ref_o, ref_l, TOL["bf16"],
                 f"batch {b} mode {mode} causal {causal} assignment {assignment}")
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("hkv", [4, 2])
+def test_prefill_odd_groups_all_launch_modes(B, mode, hkv):
+    """MHA (group size 1) and an odd group size run as row-pair work items: every
+    launch mode -- including the single launch, whose Pass-KV ordering counters
+    are indexed by 128-row tile -- gives bitwise the same result, and it
+    matches the oracle."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(77 + hkv)
+    hq = 4 if hkv == 4 else 6
+    q = torch.randn((1, 2048, hq, 128), generator=g, device="cuda").to(torch.bfloat16)
+    k = torch.randn((1, 2048, hkv, 128), generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn((1, 2048, hkv, 128), generator=g, device="cuda").to(torch.bfloat16)
+    outs = []
+    for launch in (0, 1, 2):
+        o, lse = B.prefill(q, k, v, 4, mode, launch=launch)
+        torch.cuda.synchronize()
+        assert B.device_status() == 0
+        outs.append((o, lse))
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+    rows = np.arange(2048)
+    ref_o, ref_l = oracle_rows(q, k, v, rows)
+    compare(outs[0][0], outs[0][1], rows, ref_o, ref_l, TOL["bf16"], f"odd group hkv {hkv} mode {mode}")
