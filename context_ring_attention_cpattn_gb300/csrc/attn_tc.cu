@@ -307,7 +307,8 @@ __global__ void __launch_bounds__(Layout<NT>::kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::tmem_slot_off);
 
   // ---- work item geometry (every role decodes the same items identically)
-  //   per-head tiles (pack_g == 0): (pair, query tile, head group, batch)
+  //   per-head tiles (pack_g == 0): (pair, query rows, heads, batch) -- 128
+  //     rows of a pair of heads, or 256 rows of one head with row pairs
   //   packed decode tiles (pack_g > 0, NT == 1): (pair, kv split, kv head, batch)
   struct Item {
     const PairDesc *pd;
