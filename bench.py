@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # DRAM bytes (read + write) per tensor FLOP of the tensor-core attention
 # kernel from one ncu capture, and the kernel source it was taken from; the
 # roofline's traffic is null whenever the source differs from the capture.
-TRAFFIC_RECORD = {"sha": "a94d71f1463b2c9a", "bytes_per_flop": 3.0386e-4,
+TRAFFIC_RECORD = {"sha": "c5f1b4f292d219a4", "bytes_per_flop": 3.0382e-4,
                   "capture": "profiles/attn_tc_128k_passkv_step2.md"}
 
 

@@ -33,6 +33,8 @@
 #include <math.h>
 #include <stdlib.h>
 
+#include <mutex>
+
 #include "cpattn_internal.h"
 #include "epilogue.cuh"
 #include "tmem_ldst.cuh"
@@ -824,15 +826,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
+  // Looked up once (function-local static: initialised by one thread).
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void *ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
+      return reinterpret_cast<EncodeTiledFn>(ptr);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -883,18 +886,28 @@ cudaError_t launch_nt(AttnParams &p, cudaStream_t stream) {
       !make_map(&mk, p.k, p.B, p.kv_rows_total, p.Hkv, kD, p.k_sb, p.k_ss, p.k_sh) ||
       !make_map(&mv, p.v, p.B, p.kv_rows_total, p.Hkv, kD, p.v_sb, p.v_ss, p.v_sh))
     return cudaErrorInvalidValue;
-  static int configured_device = -1;
-  static int sm_count = 0;
+  // Per device: the shared-memory attribute of this instantiation, set once,
+  // and the SM count (host threads may launch on several devices at once).
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static bool configured[kMaxDevices] = {};
+  static int sms[kMaxDevices] = {};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NT, kStrictOrder, kPersistent, kRowPair>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::alloc_bytes);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return cudaErrorInvalidDevice;
+  int sm_count = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NT, kStrictOrder, kPersistent, kRowPair>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           L::alloc_bytes);
+      if (e != cudaSuccess) return e;
+      e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      configured[dev] = true;
+    }
+    sm_count = sms[dev];
   }
   // Persistent launch: one CTA per SM (shared memory admits only one), each
   // looping over work items; otherwise one CTA per item.
