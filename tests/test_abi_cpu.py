@@ -360,3 +360,27 @@ def test_choose_mode_traffic_model(lib):
     # The 32K partial prefill: 2 MiB of K/V vs ~2 MiB of Q + returned O per hop.
     mode, kv, qq = choose(2048, 16, 32768, 1, 8)
     assert mode == B.PASS_KV and qq > kv
+
+
+def test_header_compiles_as_c_and_links(lib, tmp_path):
+    """A plain C11 program includes include/cpattn.h, links libcpattn.so and
+    calls the host-only entry points (plan, critical path, launch mode,
+    workspace size, schedule choice, status string) without a GPU."""
+    import shutil
+    import subprocess
+
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    libdir = os.path.dirname(B.library_path())
+    exe = tmp_path / "abi_from_c"
+    cmd = ["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "c", "abi_from_c.c"), "-L", libdir, "-lcpattn",
+           "-Wl,-rpath," + libdir, "-o", str(exe)]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+    env = dict(os.environ)
+    cuda_lib = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64")
+    env["LD_LIBRARY_PATH"] = cuda_lib + (":" + env["LD_LIBRARY_PATH"] if env.get("LD_LIBRARY_PATH") else "")
+    run = subprocess.run([str(exe)], capture_output=True, text=True, env=env, timeout=60)
+    assert run.returncode == 0, run.stdout + run.stderr
+    assert "FAIL" not in run.stdout
