@@ -176,3 +176,25 @@ def test_strict_mma_order_matches_default(B, case, monkeypatch):
     rows = np.arange(sq)
     ref_o, ref_l = oracle_rows(q, k, v, rows, q_base=q_off, kv_pos0=kv_off, causal=causal)
     compare(o_strict, l_strict, rows, ref_o, ref_l, TOL["bf16"], f"strict {case}")
+
+
+def test_profile_records_work_and_time(B):
+    """cpattn_profile_begin/end: one record per library launch, with the
+    kernel kind, a positive CUDA-event time and the launch's algorithmic work
+    (causal-effective FLOPs for attention, bytes for a merge)."""
+    q = rand((1, 256, 4, 128), torch.bfloat16, 31)
+    k = rand((1, 256, 2, 128), torch.bfloat16, 32)
+    v = rand((1, 256, 2, 128), torch.bfloat16, 33)
+    B.profile_begin(8)
+    try:
+        oa, la = B.partial(q, k, v, 0, 0, True, out_dtype=torch.float32)
+        ob, lb = B.partial(q, k, v, 0, 0, True, out_dtype=torch.float32)
+        B.merge_(oa, la, ob, lb)
+    finally:
+        recs = B.profile_end(8)
+    assert [r[0] for r in recs] == ["attn_tc", "attn_tc", "merge2"]
+    assert all(r[1] > 0.0 for r in recs)
+    flops = 4.0 * 128 * 4 * (256 * 257 / 2)   # 4 d hq x visible (query, key) pairs
+    assert abs(recs[0][2] - flops) <= 1e-9 * flops and abs(recs[1][2] - flops) <= 1e-9 * flops
+    merge_bytes = 3 * 256 * 4 * (128 * 4 + 4)  # read both sides, write one (fp32 O + LSE)
+    assert abs(recs[2][2] - merge_bytes) <= 1e-9 * merge_bytes
