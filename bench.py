@@ -35,11 +35,10 @@ sys.path.insert(0, ROOT)
 METRIC = "CP prefill causal TFLOP/s & % of GB300 BF16 peak; ms/layer at 128K and 1M tokens"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
-# DRAM bytes (read + write) per tensor FLOP of the tensor-core attention
-# kernel from one ncu capture, and the kernel source it was taken from; the
+# DRAM bytes (read + write) per tensor FLOP of the prefill attention kernel
+# from one ncu capture, and the kernel source it was taken from; the
 # roofline's traffic is null whenever the source differs from the capture.
-TRAFFIC_RECORD = {"sha": "c5f1b4f292d219a4", "bytes_per_flop": 3.0382e-4,
-                  "capture": "profiles/attn_tc_128k_passkv_step2.md"}
+TRAFFIC_RECORD = {"sha": None, "bytes_per_flop": None, "capture": None}
 
 
 def load_peaks():
@@ -62,7 +61,7 @@ def load_peaks():
 
 
 def kernel_sha():
-    p = os.path.join(ROOT, "context_ring_attention_cpattn_gb300", "csrc", "attn_tc.cu")
+    p = os.path.join(ROOT, "context_ring_attention_cpattn_gb300", "csrc", "attn_pair.cu")
     with open(p, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
@@ -364,6 +363,56 @@ def make_buffers(B, w, q, k, modes, launch=0):
     return outs, wss
 
 
+def custom_workload(base, args):
+    """The named workload with any command-line shape overrides applied."""
+    import dataclasses
+
+    fields = {"sq": args.seq, "skv": args.kv_seq if args.kv_seq is not None else args.seq,
+              "n_chunks": args.chunks, "hq": args.hq, "hkv": args.hkv, "head_dim": args.head_dim,
+              "dtype": args.dtype, "batch": args.batch, "q_base": args.q_base}
+    fields = {k: v for k, v in fields.items() if v is not None}
+    if args.no_causal:
+        fields["causal"] = False
+    if not fields:
+        return base
+    w = dataclasses.replace(base, **fields)
+    tag = ",".join(f"{k}={v}" for k, v in sorted(fields.items()))
+    return dataclasses.replace(w, name=f"{base.name}[{tag}]")
+
+
+def seeds_of(args):
+    return (args.seed, args.seed + 1, args.seed + 2)
+
+
+def time_workload(B, name, steps, warmup, world, modes, launch, peaks):
+    """ms per layer (median) of each schedule on a named workload, with its
+    causal-effective TFLOP/s and fraction of the bf16 peaks."""
+    import torch
+
+    from context_ring_attention_cpattn_gb300.workloads import WORKLOADS, make_qkv
+
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w, device="cuda")
+    outs, wss = make_buffers(B, w, q, k, modes, launch)
+    _, pm, _ = time_modes(B, w, q, k, v, outs, wss, steps, warmup, world, modes, launch=launch)
+    names = {B.PASS_KV: "pass_kv", B.PASS_Q: "pass_q"}
+    f = w.causal_flops()
+    out = {"flops_per_layer": f, "steps": steps, "warmup": warmup,
+           "launch_mode": ["per step", "persistent per step", "single launch"][
+               B.launch_mode(q, k, w.n_chunks, modes[0], w.q_base, w.causal, launch=launch)],
+           "dtype": w.dtype}
+    for m in modes:
+        ms = statistics.median(pm[m])
+        tf = f / (ms * 1e-3) / 1e12
+        out[names[m]] = {"ms_per_layer": ms, "tflops": tf,
+                         "frac_of_bf16_burst": tf / peaks["bf16_tflops"],
+                         "frac_of_bf16_sustained": tf / peaks.get("bf16_tflops_sustained",
+                                                                  peaks["bf16_tflops"])}
+    del q, k, v, outs, wss
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -382,6 +431,21 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=2048,
                     help="oracle rows for cpu_baseline (0 skips it)")
     ap.add_argument("--ref-rows", type=int, default=256, help="oracle rows per reference step")
+    ap.add_argument("--skip-per-workload", action="store_true",
+                    help="do not time the other configurations (tiny, Llama-3-8B, partial 32K, 1M)")
+    # Shape overrides of the main workload (any of them makes a custom workload).
+    ov = ap.add_argument_group("workload overrides")
+    ov.add_argument("--seq", type=int, help="query rows")
+    ov.add_argument("--kv-seq", type=int, help="key/value rows (default: --seq)")
+    ov.add_argument("--chunks", type=int, help="CP chunks (ranks)")
+    ov.add_argument("--hq", type=int, help="query heads")
+    ov.add_argument("--hkv", type=int, help="key/value heads")
+    ov.add_argument("--head-dim", type=int, choices=[64, 128])
+    ov.add_argument("--dtype", choices=["bf16", "fp32"])
+    ov.add_argument("--batch", type=int)
+    ov.add_argument("--q-base", type=int, help="absolute position of query row 0")
+    ov.add_argument("--no-causal", action="store_true")
+    ov.add_argument("--seed", type=int, default=1, help="Q/K/V seeds are seed, seed+1, seed+2")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: warmup raised to 3 (timing rule)", file=sys.stderr)
@@ -389,7 +453,7 @@ def main():
 
     from context_ring_attention_cpattn_gb300.workloads import WORKLOADS
 
-    w = WORKLOADS[args.workload]
+    w = custom_workload(WORKLOADS[args.workload], args)
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -408,7 +472,7 @@ def main():
     modes = {"both": (B.PASS_KV, B.PASS_Q), "kv": (B.PASS_KV,), "q": (B.PASS_Q,)}[args.schedules]
     names = {B.PASS_KV: "pass_kv", B.PASS_Q: "pass_q"}
     launch = B.LAUNCH_AUTO if args.launch is None else args.launch
-    q, k, v = make_qkv(w, device="cuda")
+    q, k, v = make_qkv(w, device="cuda", seeds=seeds_of(args))
     outs, wss = make_buffers(B, w, q, k, modes, launch)
     flops_layer = w.causal_flops()
     flops_step = len(modes) * flops_layer
@@ -437,7 +501,7 @@ def main():
         traffic = TRAFFIC_RECORD["bytes_per_flop"] * tc_flops / len(tc)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if achieved else None, "traffic": traffic,
-                "kernel": "attn_tc_kernel (tcgen05 partial attention)",
+                "kernel": "attn_pair_kernel (tcgen05 cta_group::2 partial attention)",
                 "peak_source": f"{peak_src} bf16 dense, sustained",
                 "launches_timed": len(tc), "avg_launch_ms": tc_ms / len(tc) if tc else None,
                 "share_of_step": tc_ms / elapsed if elapsed else None}
@@ -484,44 +548,48 @@ def main():
            "peak_bf16_tflops": peaks["bf16_tflops"], "peak_source": peak_src,
            "l2": "inputs larger than L2: Q and O are 512 MiB each (K/V 32 MiB each stay L2-resident, as on a CP rank)",
            "parallelism": f"replicas x{world}", "cp_ring_projection": ring}
-    mode_c, kvb, qb = B.choose_mode(q, k, w.n_chunks)
+    mode_c, kvb, qb = B.choose_mode_ex(q, k, w.n_chunks, w.q_base, w.causal)
     cfg["schedule_choice"] = {"model_picks": names[mode_c], "pass_kv_ring_bytes": kvb,
-                              "pass_q_ring_bytes": qb}
+                              "pass_q_ring_bytes": qb,
+                              "model": "cpattn_prefill_choose_mode_ex (masked ring hops)"}
     if len(modes) == 2:
         cfg["schedule_choice"]["faster_on_one_gpu"] = min(ms_layer, key=ms_layer.get)
-        # Partial prefill (2048 new tokens against a 32768-token cache), where
-        # the schedules move different amounts: the model's pick and both
-        # schedules timed (ms per layer, median).
-        wp = WORKLOADS["partial-32k"]
-        qp, kp, vp = make_qkv(wp, device="cuda")
-        outsp, wssp = make_buffers(B, wp, qp, kp, modes, launch)
-        _, pmp, _ = time_modes(B, wp, qp, kp, vp, outsp, wssp, max(10, args.steps), args.warmup,
-                               world, modes, launch=launch)
-        mode_p, kvp, qbp = B.choose_mode(qp, kp, wp.n_chunks)
-        msp = {names[m]: statistics.median(pmp[m]) for m in modes}
-        cfg["schedule_choice_partial_32k"] = {"model_picks": names[mode_p],
-                                              "pass_kv_ring_bytes": kvp, "pass_q_ring_bytes": qbp,
-                                              "ms_per_layer": msp,
-                                              "faster_on_one_gpu": min(msp, key=msp.get)}
-        del qp, kp, vp, outsp, wssp
 
-    # ---- 1M-token layer (ms/layer only)
-    if not args.skip_1m and w.name != "1m":
+    # ---- the other configurations: ms per layer of each schedule (median),
+    # 3 warm-ups each; the 1M layer is timed 5 times.
+    if not args.skip_per_workload:
         del outs, wss
         torch.cuda.empty_cache()
-        w1 = WORKLOADS["1m"]
-        q1, k1, v1 = make_qkv(w1, device="cuda")
-        outs1, wss1 = make_buffers(B, w1, q1, k1, modes, launch)
-        steps1 = max(1, args.steps // 5)
-        _, pm1, _ = time_modes(B, w1, q1, k1, v1, outs1, wss1, steps1, 1, world, modes,
-                               launch=launch)
-        ms1 = {names[m]: statistics.median(pm1[m]) for m in modes}
-        f1 = w1.causal_flops()
-        cfg["ms_per_layer_1m"] = ms1
-        cfg["tflops_per_schedule_1m"] = {k_: f1 / (v_ * 1e-3) / 1e12 for k_, v_ in ms1.items()}
-        cfg["steps_1m"] = steps1
-        del outs1, wss1, q1, k1, v1
-        torch.cuda.empty_cache()
+        per = {}
+        for name in ("tiny", "llama3-8b", "partial-32k", "128k", "1m"):
+            if name == "1m" and args.skip_1m:
+                continue
+            if name == w.name:
+                per[name] = {"flops_per_layer": flops_layer, "steps": args.steps,
+                             "warmup": args.warmup, "launch_mode": cfg["launch_mode"],
+                             "dtype": w.dtype, "see": "the main workload above"}
+                for m in modes:
+                    tf = flops_layer / (ms_layer[names[m]] * 1e-3) / 1e12
+                    per[name][names[m]] = {
+                        "ms_per_layer": ms_layer[names[m]], "tflops": tf,
+                        "frac_of_bf16_burst": tf / peaks["bf16_tflops"],
+                        "frac_of_bf16_sustained": tf / peaks.get("bf16_tflops_sustained",
+                                                                 peaks["bf16_tflops"])}
+                continue
+            steps_w = 5 if name == "1m" else max(10, args.steps)
+            per[name] = time_workload(B, name, steps_w, 3, world, modes, launch, peaks)
+        cfg["per_workload"] = per
+        if len(modes) == 2 and "partial-32k" in per:
+            wp = WORKLOADS["partial-32k"]
+            qp, kp, _ = make_qkv(wp, device="cuda")
+            mode_p, kvp, qbp = B.choose_mode_ex(qp, kp, wp.n_chunks, wp.q_base, wp.causal)
+            msp = {names[m]: per["partial-32k"][names[m]]["ms_per_layer"] for m in modes}
+            cfg["schedule_choice_partial_32k"] = {
+                "model_picks": names[mode_p], "pass_kv_ring_bytes": kvp, "pass_q_ring_bytes": qbp,
+                "ms_per_layer": msp, "faster_on_one_gpu": min(msp, key=msp.get)}
+            del qp, kp
+        if "1m" in per:
+            cfg["ms_per_layer_1m"] = {names[m]: per["1m"][names[m]]["ms_per_layer"] for m in modes}
         outs, wss = make_buffers(B, w, q, k, modes, launch)
 
     # ---- end to end through the host-buffer entry point

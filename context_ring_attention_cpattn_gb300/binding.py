@@ -16,7 +16,7 @@ PASS_KV = 1
 PASS_Q = 2
 BF16, FP32 = 0, 1
 ROLE_NAMES = {0: "store", 1: "acc_init", 2: "acc_merge", 3: "acc_final", 4: "partial"}
-KERNEL_NAMES = {1: "attn_tc", 2: "attn_simt", 3: "merge2", 4: "mergeN"}
+KERNEL_NAMES = {1: "attn_tc", 2: "attn_simt", 3: "merge2", 4: "mergeN", 5: "table"}
 
 
 class CpattnTensor(ctypes.Structure):
@@ -55,6 +55,7 @@ EXPORTED = ["cpattn_partial", "cpattn_merge", "cpattn_prefill_workspace_size", "
             "cpattn_prefill_noalloc", "cpattn_decode_workspace_size", "cpattn_decode",
             "cpattn_prefill_ex", "cpattn_prefill_workspace_size_ex", "cpattn_prefill_plan_ex",
             "cpattn_prefill_critical_path", "cpattn_prefill_choose_mode",
+            "cpattn_prefill_choose_mode_ex",
             "cpattn_status_string", "cpattn_device_status",
             "cpattn_profile_begin", "cpattn_profile_end"]
 
@@ -69,7 +70,9 @@ class CpattnError(RuntimeError):
 
 
 def library_path() -> str:
-    return _build.LIB
+    """The in-tree libcpattn.so, or the file CPATTN_LIBRARY names (a debug
+    build of the same sources, for instance)."""
+    return os.environ.get("CPATTN_LIBRARY") or _build.LIB
 
 
 def lib():
@@ -104,6 +107,8 @@ def lib():
                                          i32, ctypes.POINTER(ctypes.c_int)]
     L.cpattn_prefill_critical_path.argtypes = [i64, i64, i64, i32, i32, i32, O, dp, dp, dp]
     L.cpattn_prefill_choose_mode.argtypes = [T, T, i32, ctypes.POINTER(ctypes.c_int), dp, dp]
+    L.cpattn_prefill_choose_mode_ex.argtypes = [T, T, i64, i32, i32, O, ctypes.POINTER(ctypes.c_int),
+                                                dp, dp]
     L.cpattn_prefill_launch_mode.argtypes = [T, T, i64, i32, i32, i32, O,
                                              ctypes.POINTER(ctypes.c_int)]
     L.cpattn_decode.argtypes = [T, T, T, i64, i32, i32, f32, T, vp, vp, ctypes.c_size_t, vp]
@@ -145,12 +150,26 @@ def view(t) -> CpattnTensor:
     return CpattnTensor(t.data_ptr(), _dtype_code(t), 0, b, s, h, d, sb, ss, sh)
 
 
-def _stream(stream=None) -> int:
+def _stream(stream=None, device=None) -> int:
+    """Raw handle of `stream`, else of the current stream of `device` (the
+    device of the call's tensors)."""
     import torch
 
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return stream.cuda_stream
+
+
+def _on(t):
+    """Context that makes the device of tensor `t` current for a library call
+    (the library launches on the current device)."""
+    import contextlib
+
+    import torch
+
+    if t.device.type != "cuda":
+        return contextlib.nullcontext()
+    return torch.cuda.device(t.device)
 
 
 def partial(q, k, v, q_off: int = 0, kv_off: int = 0, causal: bool = True, scale=None,
@@ -164,17 +183,20 @@ def partial(q, k, v, q_off: int = 0, kv_off: int = 0, causal: bool = True, scale
     if lse is None:
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
     qv, kv_, vv, ov = view(q), view(k), view(v), view(out)
-    _check(lib().cpattn_partial(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv), int(q_off),
-                                int(kv_off), int(bool(causal)), float(scale or 0.0),
-                                ctypes.byref(ov), lse.data_ptr(), _stream(stream)), "cpattn_partial")
+    with _on(q):
+        _check(lib().cpattn_partial(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
+                                    int(q_off), int(kv_off), int(bool(causal)),
+                                    float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(),
+                                    _stream(stream, q.device)), "cpattn_partial")
     return out, lse
 
 
 def merge_(o_a, lse_a, o_b, lse_b, stream=None):
     """In place: (o_a, lse_a) <- LSE-merge of (o_a, lse_a) and (o_b, lse_b)."""
     av, bv = view(o_a), view(o_b)
-    _check(lib().cpattn_merge(ctypes.byref(av), lse_a.data_ptr(), ctypes.byref(bv),
-                              lse_b.data_ptr(), _stream(stream)), "cpattn_merge")
+    with _on(o_a):
+        _check(lib().cpattn_merge(ctypes.byref(av), lse_a.data_ptr(), ctypes.byref(bv),
+                                  lse_b.data_ptr(), _stream(stream, o_a.device)), "cpattn_merge")
     return o_a, lse_a
 
 
@@ -208,12 +230,13 @@ def prefill(q, k, v, n_chunks: int, mode: int, q_base: int = 0, causal: bool = T
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     qv, kv_, vv, ov = view(q), view(k), view(v), view(out)
-    _check(lib().cpattn_prefill_ex(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
-                                   int(q_base), int(n_chunks), int(mode), int(bool(causal)),
-                                   float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(), ws_ptr,
-                                   ws_len, _opts(assignment, launch, hold_ordered_waits),
-                                   _stream(stream)),
-           "cpattn_prefill_ex")
+    with _on(q):
+        _check(lib().cpattn_prefill_ex(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
+                                       int(q_base), int(n_chunks), int(mode), int(bool(causal)),
+                                       float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(),
+                                       ws_ptr, ws_len, _opts(assignment, launch, hold_ordered_waits),
+                                       _stream(stream, q.device)),
+               "cpattn_prefill_ex")
     return out, lse
 
 
@@ -242,10 +265,12 @@ def decode(q, k, v, n_chunks: int, q_base: int = 0, causal: bool = True, scale=N
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     qv, kv_, vv, ov = view(q), view(k), view(v), view(out)
-    _check(lib().cpattn_decode(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv), int(q_base),
-                               int(n_chunks), int(bool(causal)), float(scale or 0.0),
-                               ctypes.byref(ov), lse.data_ptr(), ws_ptr, ws_len, _stream(stream)),
-           "cpattn_decode")
+    with _on(q):
+        _check(lib().cpattn_decode(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
+                                   int(q_base), int(n_chunks), int(bool(causal)),
+                                   float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(), ws_ptr,
+                                   ws_len, _stream(stream, q.device)),
+               "cpattn_decode")
     return out, lse
 
 
@@ -261,10 +286,12 @@ def prefill_noalloc(q, k, v, n_chunks: int, mode: int, q_base: int = 0, causal: 
     if lse is None:
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
     qv, kv_, vv, ov = view(q), view(k), view(v), view(out)
-    _check(lib().cpattn_prefill_noalloc(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
-                                        int(q_base), int(n_chunks), int(mode), int(bool(causal)),
-                                        float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(),
-                                        _stream(stream)), "cpattn_prefill_noalloc")
+    with _on(q):
+        _check(lib().cpattn_prefill_noalloc(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
+                                            int(q_base), int(n_chunks), int(mode),
+                                            int(bool(causal)), float(scale or 0.0),
+                                            ctypes.byref(ov), lse.data_ptr(),
+                                            _stream(stream, q.device)), "cpattn_prefill_noalloc")
     return out, lse
 
 
@@ -283,12 +310,13 @@ def prefill_host(q, k, v, n_chunks, mode, out, lse, dev_scratch, q_base=0, causa
                  scale=None, stream=None):
     """End to end from host tensors: H2D copies, prefill, D2H copies, sync."""
     qv, kv_, vv, ov = view(q), view(k), view(v), view(out)
-    _check(lib().cpattn_prefill_host(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
-                                     int(q_base), int(n_chunks), int(mode), int(bool(causal)),
-                                     float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(),
-                                     dev_scratch.data_ptr(),
-                                     dev_scratch.numel() * dev_scratch.element_size(),
-                                     _stream(stream)), "cpattn_prefill_host")
+    with _on(dev_scratch):
+        _check(lib().cpattn_prefill_host(ctypes.byref(qv), ctypes.byref(kv_), ctypes.byref(vv),
+                                         int(q_base), int(n_chunks), int(mode), int(bool(causal)),
+                                         float(scale or 0.0), ctypes.byref(ov), lse.data_ptr(),
+                                         dev_scratch.data_ptr(),
+                                         dev_scratch.numel() * dev_scratch.element_size(),
+                                         _stream(stream, dev_scratch.device)), "cpattn_prefill_host")
     return out, lse
 
 
@@ -320,6 +348,20 @@ def launch_mode(q, k, n_chunks: int, mode: int, q_base: int = 0, causal: bool = 
                                             _opts(assignment, launch), ctypes.byref(out)),
            "cpattn_prefill_launch_mode")
     return out.value
+
+
+def choose_mode_ex(q, k, n_chunks: int, q_base: int = 0, causal: bool = True,
+                   assignment: int = ASSIGN_CONTIGUOUS):
+    """(mode, pass_kv_bytes, pass_q_bytes) counting only the ring hops the
+    masked ring needs; see cpattn_prefill_choose_mode_ex."""
+    m = ctypes.c_int(0)
+    kvb, qb = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    qv, kv_ = view(q), view(k)
+    _check(lib().cpattn_prefill_choose_mode_ex(ctypes.byref(qv), ctypes.byref(kv_), int(q_base),
+                                               int(n_chunks), int(bool(causal)), _opts(assignment),
+                                               ctypes.byref(m), ctypes.byref(kvb), ctypes.byref(qb)),
+           "cpattn_prefill_choose_mode_ex")
+    return m.value, kvb.value, qb.value
 
 
 def choose_mode(q, k, n_chunks: int):

@@ -12,9 +12,10 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libcpattn.so")
-SOURCES = ["api.cu", "attn_tc.cu", "attn_simt.cu", "merge.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "attn_pair.cu", "attn_tc.cu", "attn_simt.cu", "merge.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]
@@ -27,28 +28,34 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _deps() -> list[str]:
-    inc = os.path.join(os.path.dirname(PKG), "include", "cpattn.h")
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+def _deps(csrc: str) -> list[str]:
+    inc = os.path.join(INCLUDE, "cpattn.h")
+    files = [os.path.join(csrc, f) for f in os.listdir(csrc)]
     return files + [inc, os.path.abspath(__file__)]
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str, csrc: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
-    return any(os.path.getmtime(f) > t for f in _deps())
+    t = os.path.getmtime(lib)
+    return any(os.path.getmtime(f) > t for f in _deps(csrc))
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and not _stale():
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: str = OUT_DIR,
+          csrc: str = CSRC) -> str:
+    """Compile the sources in `csrc` into `out_dir`/libcpattn.so (the in-tree
+    library by default; a debug build passes its own flags and directory)."""
+    lib = os.path.join(out_dir, "libcpattn.so")
+    if not force and not _stale(lib, csrc):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-I", csrc, "-I", INCLUDE, "-c",
+               os.path.join(csrc, src),
+               "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -58,13 +65,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -13,7 +13,10 @@
 // and the N ring steps are N launches back to back on one stream.
 #include <cuda_runtime.h>
 #include <math.h>
+#include <nvtx3/nvToolsExt.h>
+#include <stdarg.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <algorithm>
@@ -125,6 +128,27 @@ double visible_pairs(int64_t q0, int64_t nq, int64_t k0, int64_t nk, bool causal
   return ramp + (double)(nq - hi) * (double)nk;
 }
 
+// ----------------------------------------------------------------- tracing
+// An NVTX range around the enqueue of each ring step, merge and entry point
+// ("cpattn pass_kv step 3", "cpattn pass_q merge", ...): profilers attribute
+// the kernels launched inside a range to it, which ties a launch list to the
+// ring's steps.  Without a tool attached a range costs a few nanoseconds.
+struct NvtxRange {
+  explicit NvtxRange(const char *fmt, ...) {
+    char buf[96];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    nvtxRangePushA(buf);
+  }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
+const char *mode_name(int mode) { return mode == CPATTN_PASS_Q ? "pass_q" : "pass_kv"; }
+
 // ----------------------------------------------------------------- profiling
 struct Profiler {
   bool armed = false;
@@ -146,6 +170,41 @@ void prof_after(cudaStream_t st, int kind, double work) {
     g_prof.work[g_prof.n] = work;
     ++g_prof.n;
   }
+}
+
+// ----------------------------------------------------------------- plan table upload
+// The single-launch mode reads its pair table from the workspace.  The table
+// travels in the parameter blocks of small fill kernels (kTableChunk entries
+// each), which the driver copies at launch: no host buffer has to outlive the
+// call, nothing waits on the host, and the upload can be captured in a graph.
+constexpr int kTableChunk = 80;
+struct TableChunk {
+  PairDesc *dst;
+  int32_t n;
+  int32_t pad;
+  PairDesc e[kTableChunk];
+};
+static_assert(sizeof(TableChunk) <= 4096, "fill kernel parameters too large");
+
+__global__ void table_fill_kernel(const __grid_constant__ TableChunk c) {
+  const int i = (int)threadIdx.x;
+  if (i < c.n) c.dst[i] = c.e[i];
+}
+
+cudaError_t upload_table(PairDesc *dst, const std::vector<PairDesc> &table, cudaStream_t st) {
+  for (size_t x0 = 0; x0 < table.size(); x0 += kTableChunk) {
+    TableChunk c;
+    memset(&c, 0, sizeof(c));
+    c.dst = dst + x0;
+    c.n = (int32_t)std::min<size_t>(kTableChunk, table.size() - x0);
+    for (int i = 0; i < c.n; ++i) c.e[i] = table[x0 + i];
+    prof_before(st);
+    table_fill_kernel<<<1, 128, 0, st>>>(c);
+    prof_after(st, CPATTN_KERNEL_TABLE, (double)c.n * sizeof(PairDesc));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // ----------------------------------------------------------------- the plan
@@ -347,6 +406,10 @@ cudaError_t launch_attn(AttnParams &p, cudaStream_t st, const cpattn_tensor *q,
   }
   if (vis_override >= 0.0) vis = vis_override;
   const double flops = 4.0 * (double)q->d * (double)q->h * (double)q->b * vis;
+  // Kernel-side waits give up after 2 s, or after four times the launch's
+  // whole work at 100 TFLOP/s when that is longer (a wait in a persistent
+  // launch can last as long as other CTAs' items).
+  p.wait_ns = (uint64_t)std::max(2e9, 4.0 * flops / 1e14 * 1e9);
   const bool tc = attn_tc_supported(p);
   prof_before(st);
   cudaError_t e = tc ? launch_attn_tc(p, st) : launch_attn_simt(p, st);
@@ -467,6 +530,7 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
   };
 
   if (lmode == CPATTN_LAUNCH_SINGLE && attn_tc_supported(p)) {
+    NvtxRange range("cpattn %s ring, one launch", mode_name(mode));
     // One persistent launch for every ring step.  Work items keep the ring's
     // launch order; a Pass-KV accumulator update waits (bounded) until the
     // previous visit of the same rows has finished.
@@ -496,9 +560,7 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
       if ((*on_inputs)(i, 0) != cudaSuccess) return CPATTN_ERR_CUDA;
     if (total > 0) {
       PairDesc *dev_table = reinterpret_cast<PairDesc *>(ws + wl.table);
-      if (cudaMemcpyAsync(dev_table, table.data(), table.size() * sizeof(PairDesc),
-                          cudaMemcpyHostToDevice, st) != cudaSuccess)
-        return CPATTN_ERR_CUDA;
+      if (upload_table(dev_table, table, st) != cudaSuccess) return CPATTN_ERR_CUDA;
       p.pair_table = dev_table;
       p.n_table = (int32_t)table.size();
       p.total_ctas = total;
@@ -550,6 +612,7 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
       ++mp.n_items;
     }
     if (mp.n_items == 0) return CPATTN_OK;
+    NvtxRange range("cpattn %s merge", mode_name(mode));
     prof_before(st);
     cudaError_t e = launch_merge_n(mp, st);
     prof_after(st, CPATTN_KERNEL_MERGEN, bytes);
@@ -574,6 +637,7 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
     size_t e1 = e0;
     while (e1 < pl.entries.size() && pl.entries[e1].launch == l) ++e1;
     if (e1 == e0) continue;
+    NvtxRange range("cpattn %s step %d", mode_name(mode), pl.entries[e0].step);
     std::vector<PairDesc> items;
     launch_items(e0, e1, items);
     if (on_inputs != nullptr && l == 0) {
@@ -729,6 +793,7 @@ cpattn_status cpattn_partial(const cpattn_tensor *q, const cpattn_tensor *k,
         kv_off > kMaxRows * 4)
       return CPATTN_ERR_UNSUPPORTED;
     if (q->s == 0) return CPATTN_OK;
+    NvtxRange range("cpattn partial");
     AttnParams p;
     fill_inputs(p, q, k, v, causal, scale);
     p.out = out_view(o, lse);
@@ -770,6 +835,7 @@ cpattn_status cpattn_merge(cpattn_tensor *o_a, float *lse_a, const cpattn_tensor
   p.a = out_view(o_a, lse_a);
   p.b = out_view(o_b, const_cast<float *>(lse_b));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  NvtxRange range("cpattn merge");
   const double bytes = 3.0 * (double)o_a->b * o_a->s * o_a->h * (o_a->d * elem_bytes(o_a->dtype) + 4.0);
   prof_before(st);
   cudaError_t e = launch_merge_2(p, st);
@@ -879,6 +945,7 @@ cpattn_status cpattn_decode(const cpattn_tensor *q, const cpattn_tensor *k, cons
       if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return CPATTN_ERR_WORKSPACE;
     }
     if (q->s == 0) return CPATTN_OK;
+    NvtxRange range("cpattn decode");
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
     AttnParams p;
@@ -953,6 +1020,64 @@ cpattn_status cpattn_prefill_choose_mode(const cpattn_tensor *q, const cpattn_te
   if (pass_kv_bytes) *pass_kv_bytes = kv;
   if (pass_q_bytes) *pass_q_bytes = qb;
   return CPATTN_OK;
+}
+
+cpattn_status cpattn_prefill_choose_mode_ex(const cpattn_tensor *q, const cpattn_tensor *k,
+                                            int64_t q_base, int n_chunks, int causal,
+                                            const cpattn_prefill_options *opts, int *mode,
+                                            double *pass_kv_bytes, double *pass_q_bytes) {
+  try {
+    if (mode == nullptr || q == nullptr || k == nullptr) return CPATTN_ERR_INVALID_ARG;
+    const int es = elem_bytes(q->dtype);
+    if (es == 0 || q->h < 1 || k->h < 1 || q->d < 1 || q->b < 1) return CPATTN_ERR_INVALID_ARG;
+    Plan pl;
+    cpattn_status s =
+        build_plan(q->s, k->s, q_base, n_chunks, CPATTN_PASS_KV, causal, assignment_of(opts), pl);
+    if (s != CPATTN_OK) return s;
+    const int N = pl.N;
+    const bool cz = causal != 0;
+    // need[r * N + s]: some Q piece of rank r sees some K/V piece of rank s.
+    std::vector<char> need((size_t)N * N, 0);
+    int64_t remote_pairs = 0;  // visible piece pairs whose Q and K/V live on different ranks
+    for (int r = 0; r < N; ++r)
+      for (int t = 0; t < N; ++t) {
+        int qp[2], kp[2];
+        const int nq = rank_pieces(pl, r, qp), nk = rank_pieces(pl, t, kp);
+        for (int a = 0; a < nq; ++a)
+          for (int b = 0; b < nk; ++b)
+            if (pair_visible(pl, q_base, cz, qp[a], kp[b])) {
+              need[(size_t)r * N + t] = 1;
+              if (r != t) ++remote_pairs;
+            }
+      }
+    // A travelling chunk moves one rank per step in the ring's direction (rank
+    // r receives the chunk of rank (r - 1) mod N) until the farthest rank that
+    // needs it has it.
+    const int ppr = pl.P / N;  // pieces per rank
+    const double kv_unit = (double)ppr * pl.C * k->h * q->d * es * 2.0 * q->b;
+    const double q_unit = (double)ppr * pl.Cq * q->h * q->d * es * (double)q->b;
+    const double ret_unit = (double)pl.Cq * q->h * ((double)q->d * es + 4.0) * q->b;
+    double kv = 0.0, qb = 0.0;
+    for (int t = 0; t < N; ++t) {  // K/V of rank t travel to the ranks whose Q sees them
+      int hops = 0;
+      for (int r = 0; r < N; ++r)
+        if (r != t && need[(size_t)r * N + t]) hops = std::max(hops, ((r - t) % N + N) % N);
+      kv += hops * kv_unit;
+    }
+    for (int r = 0; r < N; ++r) {  // Q of rank r travels to the ranks whose K/V it sees
+      int hops = 0;
+      for (int t = 0; t < N; ++t)
+        if (t != r && need[(size_t)r * N + t]) hops = std::max(hops, ((t - r) % N + N) % N);
+      qb += hops * q_unit;
+    }
+    qb += (double)remote_pairs * ret_unit;  // each remote partial (O, LSE) returns once
+    *mode = qb < kv ? CPATTN_PASS_Q : CPATTN_PASS_KV;
+    if (pass_kv_bytes) *pass_kv_bytes = kv;
+    if (pass_q_bytes) *pass_q_bytes = qb;
+    return CPATTN_OK;
+  } catch (...) {
+    return CPATTN_ERR_INVALID_ARG;
+  }
 }
 
 cpattn_status cpattn_prefill_plan(int64_t sq, int64_t skv, int64_t q_base, int n_chunks, int mode,
@@ -1047,6 +1172,7 @@ cpattn_status cpattn_prefill_host(const cpattn_tensor *q, const cpattn_tensor *k
     if (dev_scratch == nullptr || scratch_bytes < need ||
         reinterpret_cast<uintptr_t>(dev_scratch) % 256 != 0)
       return CPATTN_ERR_WORKSPACE;
+    NvtxRange range("cpattn prefill_host %s", mode_name(mode));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *base = reinterpret_cast<uint8_t *>(dev_scratch);
     size_t off = 0;

@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/cpattn.h"
+#include "cpattn.h"
 
 namespace cpattn {
 
@@ -80,6 +80,9 @@ struct AttnParams {
   // bounded wait run out when testing failure detection).
   int32_t *dep_counters;
   int32_t dep_hold;
+  // Bound of every kernel-side wait, in ns of global time (set by the
+  // launcher from the launch's planned work; at least 2 s).
+  uint64_t wait_ns;
   OutView out;              // final output (absolute q rows)
   OutView acc;              // Pass-KV fp32 accumulator (absolute q rows)
   OutView part;             // Pass-Q slot 0 (chunk-relative rows)
@@ -110,13 +113,19 @@ struct Merge2Params {
 };
 
 // Launchers (return cudaSuccess or the launch error).
+//   launch_attn_tc     tensor-core kernels: per-head tiles (pack_g == 0) on a
+//                      CTA pair (attn_pair.cu), packed decode tiles
+//                      (pack_g > 0) on one CTA (attn_tc.cu)
 cudaError_t launch_attn_tc(AttnParams &p, cudaStream_t stream);
+cudaError_t launch_attn_pair(AttnParams &p, cudaStream_t stream);
+cudaError_t launch_attn_decode_tc(AttnParams &p, cudaStream_t stream);
 cudaError_t launch_attn_simt(AttnParams &p, cudaStream_t stream);
 cudaError_t launch_merge_n(const MergeNParams &p, cudaStream_t stream);
 cudaError_t launch_merge_2(const Merge2Params &p, cudaStream_t stream);
 
-// True when the tensor-core kernel supports these shapes.
+// True when a tensor-core kernel supports these shapes.
 bool attn_tc_supported(const AttnParams &p);
+bool attn_decode_tc_supported(const AttnParams &p);
 // Per-head work items of the tensor-core kernel (pack_g == 0): query rows
 // and heads per item -- 128 rows of 2 heads sharing a kv head when Hq / Hkv
 // is even, else 256 rows (two 128-row tiles) of 1 head.
@@ -125,7 +134,9 @@ struct TcItemShape {
 };
 TcItemShape attn_tc_item_shape(const AttnParams &p);
 
-// Device status words (one per translation unit that has bounded waits).
+// Device status words (one per translation unit that has bounded waits);
+// attn_tc_read_status reads (and clears) both tensor-core kernels' words.
 unsigned int attn_tc_read_status(bool clear, cudaError_t *err);
+unsigned int attn_pair_read_status(bool clear, cudaError_t *err);
 
 }  // namespace cpattn

@@ -110,10 +110,22 @@ struct RowSink {
   const float *acc;  // accumulator row read by the merge roles
   float wa, wb;    // merge weights (merge roles)
 
+  // The accumulator LSE a merge role combines with (-inf for other roles).
+  // When several threads share a row, each reads it before any of them
+  // writes the merged LSE in place, and passes it to init().
+  __device__ static __forceinline__ float acc_lse(const AttnParams &p, const PairDesc &pd, int b,
+                                                  int h, int rel_row) {
+    if (pd.mode != kAccMerge && pd.mode != kAccFinal) return -INFINITY;
+    return *view_lse(p.acc, b, (int64_t)pd.q_row0 + rel_row, h);
+  }
+
   // rel_row: row inside the pair's q chunk.  lse_p: the partial's LSE.
   // write_lse: this thread writes the LSE (one thread per row and head).
+  // acc_lse_old: the accumulator LSE read beforehand (acc_lse), or null to
+  // read it here.
   __device__ __forceinline__ void init(const AttnParams &p, const PairDesc &pd, int b, int h,
-                                       int rel_row, float lse_p, bool write_lse, int slot = -1) {
+                                       int rel_row, float lse_p, bool write_lse, int slot = -1,
+                                       const float *acc_lse_old = nullptr) {
     mode = pd.mode;
     if (slot < 0) slot = pd.slot;
     const int64_t abs_row = (int64_t)pd.q_row0 + rel_row;
@@ -138,7 +150,7 @@ struct RowSink {
     } else {  // kAccMerge / kAccFinal
       float *acc_lse = view_lse(p.acc, b, abs_row, h);
       acc = reinterpret_cast<const float *>(view_row(p.acc, b, abs_row, h));
-      const MergeW mw = merge_weights(*acc_lse, lse_p);
+      const MergeW mw = merge_weights(acc_lse_old != nullptr ? *acc_lse_old : *acc_lse, lse_p);
       wa = mw.wa;
       wb = mw.wb;
       if (mode == kAccMerge) {

@@ -9,12 +9,11 @@
 // afterwards; reading notes, section "The communication bottleneck across all
 // three axes", CP paragraph: ranks accumulate the full attention result).
 //
-// Mapping: one warp per (batch, row, head) vector of D values, lanes own D/32
-// consecutive columns (16-byte fp32 loads at D = 128), consecutive warps walk
-// consecutive rows of the [b, s, h, d] layout, so every request is a fully
-// used, coalesced 512-byte line.  Grids cover all rows with short CTAs (no
-// grid-stride loop), so uneven per-row work is balanced by the scheduler.
-// fp32 arithmetic, output rounded once.
+// Mapping: a warp merges whole (batch, row, head) vectors of D values, lanes
+// owning D/32 consecutive columns (16-byte fp32 loads at D = 128), so every O
+// request is a fully used, coalesced 512-byte line.  Grids cover all rows with
+// short CTAs (no grid-stride loop), so uneven per-row work is balanced by the
+// scheduler.  fp32 arithmetic, output rounded once.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -25,7 +24,7 @@ namespace cpattn {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kRowsPerWarp = 2;  // pairwise merge: rows per warp, all their loads in flight together
+constexpr int kRowsInFlight = 4;  // pairwise merge: rows per warp with all their loads in flight
 
 template <int E>
 __device__ __forceinline__ void load_row(const OutView &w, int b, int64_t row, int h, int c0,
@@ -40,39 +39,52 @@ __device__ __forceinline__ void load_row(const OutView &w, int b, int64_t row, i
   }
 }
 
-// (a) <- merge(a, b), element-wise over rows.  Each warp merges kRowsPerWarp
-// rows with all their loads issued before any arithmetic.
+// (a) <- merge(a, b), element-wise over rows.  One warp per run of 32
+// consecutive rows of one (batch, head): lane l reads the two LSEs of row
+// s0 + l (one coalesced 128-byte load per side, contiguous in the [b, h, s]
+// layout), computes that row's weights and writes its merged LSE; the rows'
+// O vectors (lanes own D/32 consecutive columns) are then merged
+// kRowsInFlight at a time with every load issued before any arithmetic, the
+// weights broadcast from the row's lane.
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32) merge2_kernel(const __grid_constant__ Merge2Params p) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
-  const int64_t n_rows = (int64_t)p.B * p.S * p.H;
-  const int64_t r0 = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRowsPerWarp;
-  float va[kRowsPerWarp][E], vb[kRowsPerWarp][E], la[kRowsPerWarp], lb[kRowsPerWarp];
-  int hh[kRowsPerWarp], bb[kRowsPerWarp];
-  int64_t ss[kRowsPerWarp];
-#pragma unroll
-  for (int u = 0; u < kRowsPerWarp; ++u) {
-    const int64_t r = r0 + u;
-    if (r >= n_rows) break;
-    hh[u] = (int)(r % p.H);
-    ss[u] = (r / p.H) % p.S;
-    bb[u] = (int)(r / ((int64_t)p.H * p.S));
-    la[u] = *view_lse(p.a, bb[u], ss[u], hh[u]);
-    lb[u] = *view_lse(p.b, bb[u], ss[u], hh[u]);
-    load_row<E>(p.a, bb[u], ss[u], hh[u], lane * E, va[u]);
-    load_row<E>(p.b, bb[u], ss[u], hh[u], lane * E, vb[u]);
+  const int64_t n_runs = ((int64_t)p.S + 31) / 32;
+  const int64_t wid = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (wid >= (int64_t)p.B * p.H * n_runs) return;
+  const int64_t s0 = (wid % n_runs) * 32;
+  const int h = (int)((wid / n_runs) % p.H);
+  const int b = (int)(wid / (n_runs * p.H));
+  const int nrow = (int)((int64_t)p.S - s0 < 32 ? (int64_t)p.S - s0 : 32);
+  float la = -INFINITY, lb = -INFINITY;
+  if (lane < nrow) {
+    la = *view_lse(p.a, b, s0 + lane, h);
+    lb = *view_lse(p.b, b, s0 + lane, h);
   }
+  const MergeW w = merge_weights(la, lb);
+#pragma unroll 1
+  for (int u0 = 0; u0 < nrow; u0 += kRowsInFlight) {
+    float va[kRowsInFlight][E], vb[kRowsInFlight][E];
 #pragma unroll
-  for (int u = 0; u < kRowsPerWarp; ++u) {
-    if (r0 + u >= n_rows) break;
-    const MergeW w = merge_weights(la[u], lb[u]);
+    for (int u = 0; u < kRowsInFlight; ++u) {
+      if (u0 + u < nrow) {
+        load_row<E>(p.a, b, s0 + u0 + u, h, lane * E, va[u]);
+        load_row<E>(p.b, b, s0 + u0 + u, h, lane * E, vb[u]);
+      }
+    }
 #pragma unroll
-    for (int i = 0; i < E; ++i) va[u][i] = __fmul_rn(w.wa, va[u][i]) + __fmul_rn(w.wb, vb[u][i]);
-    __syncwarp();
-    store_vals<E>(view_row(p.a, bb[u], ss[u], hh[u]), p.a.f32, lane * E, va[u]);
-    if (lane == 0) *view_lse(p.a, bb[u], ss[u], hh[u]) = w.lse;
+    for (int u = 0; u < kRowsInFlight; ++u) {
+      if (u0 + u < nrow) {  // warp-uniform
+        const float wa = __shfl_sync(0xffffffffu, w.wa, u0 + u);
+        const float wb = __shfl_sync(0xffffffffu, w.wb, u0 + u);
+#pragma unroll
+        for (int i = 0; i < E; ++i) va[u][i] = __fmul_rn(wa, va[u][i]) + __fmul_rn(wb, vb[u][i]);
+        store_vals<E>(view_row(p.a, b, s0 + u0 + u, h), p.a.f32, lane * E, va[u]);
+      }
+    }
   }
+  if (lane < nrow) *view_lse(p.a, b, s0 + lane, h) = w.lse;
 }
 
 // Pass-Q: for item x, rows [0, chunk_rows) of Q chunk x merge slots
@@ -263,10 +275,9 @@ __global__ void __launch_bounds__(kWarps * 32)
 }  // namespace
 
 cudaError_t launch_merge_2(const Merge2Params &p, cudaStream_t stream) {
-  const int64_t n_rows = (int64_t)p.B * p.S * p.H;
-  if (n_rows == 0) return cudaSuccess;
-  const int64_t per_cta = (int64_t)kWarps * kRowsPerWarp;
-  const int64_t grid = (n_rows + per_cta - 1) / per_cta;
+  const int64_t n_warps = (int64_t)p.B * p.H * (((int64_t)p.S + 31) / 32);
+  if (n_warps == 0) return cudaSuccess;
+  const int64_t grid = (n_warps + kWarps - 1) / kWarps;
   if (p.D == 128) {
     merge2_kernel<128><<<(unsigned)grid, kWarps * 32, 0, stream>>>(p);
   } else if (p.D == 64) {

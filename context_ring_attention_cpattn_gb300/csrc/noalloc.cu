@@ -18,7 +18,7 @@
 
 #include <mutex>
 
-#include "../../include/cpattn.h"
+#include "cpattn.h"
 
 namespace {
 

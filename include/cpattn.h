@@ -26,8 +26,12 @@
  * Ownership and concurrency: the caller owns every buffer (inputs, outputs
  * and workspace are device memory unless stated).  The library never
  * allocates device memory, never frees, never synchronises the stream it is
- * given: every compute call only enqueues kernels on `stream` (a
- * cudaStream_t; NULL = legacy default stream) and returns.
+ * given: every device-buffer compute call only enqueues kernels (and, for a
+ * single-launch Pass-KV ring, one device memset of its progress counters) on
+ * `stream` (a cudaStream_t; NULL = legacy default stream) and returns.  No
+ * such call copies from host memory, so none waits on the host, and each can
+ * be captured into a CUDA graph.  cpattn_prefill_host is the exception: its
+ * contract is to copy host buffers and return finished results.
  *
  * Errors: argument errors are detected on the host before anything is
  * enqueued and return CPATTN_ERR_INVALID_ARG / CPATTN_ERR_UNSUPPORTED /
@@ -303,6 +307,28 @@ cpattn_status cpattn_prefill_choose_mode(const cpattn_tensor *q, const cpattn_te
                                          double *pass_q_bytes);
 
 /*
+ * cpattn_prefill_choose_mode_ex -- the same choice for the ring that
+ * cpattn_prefill_ex actually runs (q_base, causal mask, chunk-to-rank
+ * assignment of `opts`; host only).  A chunk travels only as far as the
+ * ring needs it: at step t rank r holds the travelling chunk of rank
+ * (r - t) mod N, so the chunk of rank s makes max (r - s) mod N hops over the
+ * ranks r whose pairs with it have a visible key (0 if none).  With a causal
+ * mask and contiguous chunks K/V therefore travel N (N-1) / 2 hops in all,
+ * Q (N-1)^2 (a Q chunk sees the ranks before it, which the ring reaches
+ * last).  Bytes:
+ *   Pass-KV = sum over ranks of hops * 2 * (pieces per rank) * C_kv * hkv * d * es * b
+ *   Pass-Q  = sum over ranks of hops * (pieces per rank) * C_q * hq * d * es * b
+ *             + (visible piece pairs on different ranks) * C_q * hq * (d * es + 4) * b
+ *             (each remote partial O and its LSE return to the Q owner once)
+ * with C_kv, C_q the piece lengths.  *mode receives the cheaper schedule (ties
+ * go to Pass-KV); either byte count pointer may be NULL.
+ */
+cpattn_status cpattn_prefill_choose_mode_ex(const cpattn_tensor *q, const cpattn_tensor *k,
+                                            int64_t q_base, int n_chunks, int causal,
+                                            const cpattn_prefill_options *opts, int *mode,
+                                            double *pass_kv_bytes, double *pass_q_bytes);
+
+/*
  * cpattn_prefill_host -- end-to-end convenience: q, k, v, o are HOST tensors
  * (pageable or pinned); lse is a host array [b, hq, sq].  Copies inputs to
  * device staging buffers the caller provides (`dev_scratch`, at least
@@ -372,7 +398,8 @@ typedef enum {
   CPATTN_KERNEL_ATTN_TC = 1,    /* tcgen05 partial-attention kernel */
   CPATTN_KERNEL_ATTN_SIMT = 2,  /* fp32 / head_dim 64 partial-attention kernel */
   CPATTN_KERNEL_MERGE2 = 3,     /* pairwise LSE merge */
-  CPATTN_KERNEL_MERGEN = 4      /* N-way LSE merge of Pass-Q partials */
+  CPATTN_KERNEL_MERGEN = 4,     /* N-way LSE merge of Pass-Q partials */
+  CPATTN_KERNEL_TABLE = 5       /* pair-table upload of a single-launch ring (work = bytes) */
 } cpattn_kernel_kind;
 
 typedef struct {

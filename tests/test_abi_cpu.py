@@ -362,6 +362,66 @@ def test_choose_mode_traffic_model(lib):
     assert mode == B.PASS_KV and qq > kv
 
 
+def choose_ex(lib, sq, hq, skv, hkv, n, q_base=0, causal=True, assignment=B.ASSIGN_CONTIGUOUS,
+              d=128):
+    m, kvb, qb = ctypes.c_int(), ctypes.c_double(), ctypes.c_double()
+    q, k = T(s=sq, h=hq, d=d), T(s=skv, h=hkv, d=d)
+    assert lib.cpattn_prefill_choose_mode_ex(ctypes.byref(q), ctypes.byref(k), q_base, n,
+                                             int(causal), B._opts(assignment), ctypes.byref(m),
+                                             ctypes.byref(kvb), ctypes.byref(qb)) == 0
+    return m.value, kvb.value, qb.value
+
+
+def test_choose_mode_ex_causal_hops(lib):
+    """Hand-counted ring traffic.  Causal self-prefill, 4 contiguous chunks:
+    K/V chunk j is needed by ranks j+1..3, which the ring reaches first, so
+    the chunks make 3 + 2 + 1 + 0 = 6 hops; Q chunk i needs ranks 0..i-1,
+    which the ring reaches last, so Q chunks 1, 2, 3 make 3 hops each (9);
+    6 remote pairs return a partial.  Without the mask every chunk makes 3
+    hops and 12 pairs return."""
+    c = 256 // 4
+    kv_chunk = 2 * c * 1 * 128 * 2          # K and V of one chunk, 1 kv head, bf16
+    q_chunk = c * 4 * 128 * 2               # Q of one chunk, 4 q heads
+    ret = c * 4 * (128 * 2 + 4)             # one partial O (bf16) and its LSE
+    mode, kv, qq = choose_ex(lib, 256, 4, 256, 1, 4)
+    assert kv == 6 * kv_chunk and qq == 9 * q_chunk + 6 * ret and mode == B.PASS_KV
+    mode, kv, qq = choose_ex(lib, 256, 4, 256, 1, 4, causal=False)
+    assert kv == 12 * kv_chunk and qq == 12 * q_chunk + 12 * ret
+    # A single chunk never travels.
+    assert choose_ex(lib, 256, 4, 256, 1, 1)[1:] == (0.0, 0.0)
+
+
+def test_choose_mode_ex_partial_prefill_and_decode(lib):
+    """Partial prefill (2048 new tokens at 30720.. against 32768 cached keys,
+    8 ranks): every new token sees every cached chunk, so each chunk makes all
+    7 hops and all 56 remote pairs return -- the same counts as the unmasked
+    model.  A decode-shaped query (16 tokens at the end of a 128K cache)
+    travels as Q."""
+    mode, kv, qq = choose_ex(lib, 2048, 16, 32768, 1, 8, q_base=30720)
+    assert kv == 8 * 7 * 2 * 4096 * 128 * 2
+    assert qq == 8 * 7 * 256 * 16 * 128 * 2 + 56 * 256 * 16 * (128 * 2 + 4)
+    assert mode == B.PASS_KV
+    mode, kv, qq = choose_ex(lib, 16, 16, 131072, 1, 16, q_base=131072 - 16)
+    assert mode == B.PASS_Q and qq < kv
+
+
+def test_choose_mode_ex_zigzag(lib):
+    """Zigzag pieces (rank r holds r and 2N-1-r): every rank's Q sees every
+    rank's K/V, so both schedules use all N-1 hops per rank, each hop moving
+    two pieces."""
+    n, s = 4, 512
+    p = s // (2 * n)
+    mode, kv, qq = choose_ex(lib, s, 4, s, 1, n, assignment=B.ASSIGN_ZIGZAG)
+    assert kv == n * (n - 1) * 2 * p * 1 * 128 * 2 * 2
+    visible_remote = 0
+    pieces = lambda r: (r, 2 * n - 1 - r)
+    for r in range(n):
+        for t in range(n):
+            if r != t:
+                visible_remote += sum(1 for a in pieces(r) for b in pieces(t) if b * p <= a * p + p - 1)
+    assert qq == n * (n - 1) * 2 * p * 4 * 128 * 2 + visible_remote * p * 4 * (128 * 2 + 4)
+
+
 def test_header_compiles_as_c_and_links(lib, tmp_path):
     """A plain C11 program includes include/cpattn.h, links libcpattn.so and
     calls the host-only entry points (plan, critical path, launch mode,

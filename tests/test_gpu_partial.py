@@ -154,28 +154,25 @@ def test_argument_errors_do_not_launch(B):
     assert err.value.status == 2   # head_dim 96 unsupported
 
 
-@pytest.mark.parametrize("case", [TC_CASES[1], TC_CASES[2], TC_CASES[3], TC_CASES[4], TC_CASES[5],
-                                  (300, 2000, 3, 3, 128, 1700, 0, True)],
-                         ids=lambda c: "x".join(map(str, c)))
-def test_strict_mma_order_matches_default(B, case, monkeypatch):
-    """The default MMA schedule lets a QK product follow the PV MMA that reads
-    the same TMEM columns without waiting (it relies on the tensor pipe running
-    one thread's MMAs in issue order).  CPATTN_STRICT_MMA_ORDER=1 waits for
-    each PV MMA instead.  Both must give bitwise the same result, and both must
-    match the oracle.  Hq == Hkv cases run the one-tile kernel with two score
-    buffers."""
-    sq, skv, hq, hkv, d, q_off, kv_off, causal = case
-    q = rand((1, sq, hq, d), torch.bfloat16, 21)
-    k = rand((1, skv, hkv, d), torch.bfloat16, 22)
-    v = rand((1, skv, hkv, d), torch.bfloat16, 23)
-    o_fast, l_fast = B.partial(q, k, v, q_off, kv_off, causal, out_dtype=torch.float32)
-    monkeypatch.setenv("CPATTN_STRICT_MMA_ORDER", "1")
-    o_strict, l_strict = B.partial(q, k, v, q_off, kv_off, causal, out_dtype=torch.float32)
+@pytest.mark.parametrize("hq,hkv", [(4, 1), (3, 3)], ids=["head_pairs", "row_pairs"])
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+def test_partial_growing_logits_rescale(B, hq, hkv, out_dtype):
+    """Keys whose scale grows along the sequence make every row's running
+    maximum grow by more than the lazy-rescale threshold again and again, so
+    O is rescaled in TMEM at many KV steps (the softmax then waits for the
+    previous step's PV MMA): every row against the oracle."""
+    sq, skv = 640, 1536
+    q = rand((1, sq, hq, 128), torch.bfloat16, 41)
+    ramp = (1.0 + torch.arange(skv, device="cuda", dtype=torch.float32) / 48.0).view(1, skv, 1, 1)
+    k = (rand((1, skv, hkv, 128), torch.float32, 42) * ramp).to(torch.bfloat16)
+    v = rand((1, skv, hkv, 128), torch.bfloat16, 43)
+    od = torch.bfloat16 if out_dtype == "bf16" else torch.float32
+    o, lse = B.partial(q, k, v, skv - sq, 0, True, out_dtype=od)
     torch.cuda.synchronize()
-    assert torch.equal(o_fast, o_strict) and torch.equal(l_fast, l_strict)
+    assert B.device_status() == 0
     rows = np.arange(sq)
-    ref_o, ref_l = oracle_rows(q, k, v, rows, q_base=q_off, kv_pos0=kv_off, causal=causal)
-    compare(o_strict, l_strict, rows, ref_o, ref_l, TOL["bf16"], f"strict {case}")
+    ref_o, ref_l = oracle_rows(q, k, v, rows, q_base=skv - sq)
+    compare(o, lse, rows, ref_o, ref_l, TOL["bf16"], f"growing logits {hq}/{hkv}")
 
 
 def test_profile_records_work_and_time(B):
