@@ -41,10 +41,17 @@ def _stale(lib: str, csrc: str) -> bool:
     return any(os.path.getmtime(f) > t for f in _deps(csrc))
 
 
+DEBUG_DIR = os.path.join(PKG, "_build_debug")
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: str = OUT_DIR,
-          csrc: str = CSRC) -> str:
+          csrc: str = CSRC, debug: bool = False) -> str:
     """Compile the sources in `csrc` into `out_dir`/libcpattn.so (the in-tree
-    library by default; a debug build passes its own flags and directory)."""
+    library by default).  debug=True builds the same sources with
+    -DCPATTN_DEBUG (kernel bounds checks) into _build_debug/."""
+    if debug:
+        extra_flags = (*extra_flags, "-DCPATTN_DEBUG")
+        out_dir = DEBUG_DIR if out_dir == OUT_DIR else out_dir
     lib = os.path.join(out_dir, "libcpattn.so")
     if not force and not _stale(lib, csrc):
         return lib

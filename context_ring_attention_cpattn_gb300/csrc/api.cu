@@ -492,6 +492,9 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
     p.acc.lb = q->h * q->s;
     p.acc.f32 = 1;
   }
+  p.n_part_slots = pl.n_slots;
+  p.part_rows = (int32_t)pl.Cq;
+  p.n_dep_counters = (int32_t)wl.n_counters;
   if (pl.n_slots > 0) {
     p.part.o = ws + wl.part_o;
     p.part.lse = reinterpret_cast<float *>(ws + wl.part_lse);
@@ -592,6 +595,7 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
   mp.part = p.part;
   mp.part_o_stride = p.part_o_stride;
   mp.part_lse_stride = p.part_lse_stride;
+  mp.n_part_slots = pl.n_slots;
   const double row_bytes = (double)q->b * pl.Cq * q->h * (q->d * 4.0 + 4.0);
   const double out_bytes = (double)q->b * pl.Cq * q->h * (q->d * elem_bytes(o->dtype) + 4.0);
   auto needs_merge_launch = [&](int i) {
@@ -778,6 +782,8 @@ const char *cpattn_status_string(cpattn_status s) {
     case CPATTN_ERR_WORKSPACE: return "CPATTN_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case CPATTN_ERR_CUDA: return "CPATTN_ERR_CUDA: a CUDA call or launch failed";
     case CPATTN_ERR_TIMEOUT: return "CPATTN_ERR_TIMEOUT: a kernel-side wait gave up";
+    case CPATTN_ERR_DEVICE_CHECK:
+      return "CPATTN_ERR_DEVICE_CHECK: a debug-build kernel bounds check failed";
   }
   return "CPATTN: unknown status";
 }
@@ -963,6 +969,8 @@ cpattn_status cpattn_decode(const cpattn_tensor *q, const cpattn_tensor *k, cons
       p.part.f32 = 1;
       p.part_o_stride = q->b * q->s * q->h * q->d;
       p.part_lse_stride = q->b * q->h * q->s;
+      p.n_part_slots = dp.n_slots;
+      p.part_rows = (int32_t)q->s;
       p.n_pairs = (int32_t)dp.chunk.size();
       for (size_t x = 0; x < dp.chunk.size(); ++x) {
         PairDesc &pd = p.pairs[x];
@@ -995,6 +1003,7 @@ cpattn_status cpattn_decode(const cpattn_tensor *q, const cpattn_tensor *k, cons
     mp.item_row0[0] = 0;
     mp.item_slot0[0] = 0;
     mp.item_count[0] = dp.n_slots;
+    mp.n_part_slots = dp.n_slots;
     const double bytes = (double)dp.n_slots * q->b * q->s * q->h * (q->d * 4.0 + 4.0) +
                          (double)q->b * q->s * q->h * (q->d * elem_bytes(o->dtype) + 4.0);
     prof_before(st);
@@ -1263,10 +1272,16 @@ cpattn_status cpattn_prefill_host(const cpattn_tensor *q, const cpattn_tensor *k
 
 cpattn_status cpattn_device_status(int clear) {
   if (cudaDeviceSynchronize() != cudaSuccess) return CPATTN_ERR_CUDA;
-  cudaError_t e = cudaSuccess;
-  const unsigned int v = attn_tc_read_status(clear != 0, &e);
-  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
-  return v ? CPATTN_ERR_TIMEOUT : CPATTN_OK;
+  unsigned int (*readers[])(bool, cudaError_t *) = {attn_tc_read_status, attn_pair_read_status,
+                                                     attn_simt_read_status, merge_read_status};
+  unsigned int v = 0;
+  for (auto rd : readers) {
+    cudaError_t e = cudaSuccess;
+    v |= rd(clear != 0, &e);
+    if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  }
+  if (v & kStatusTimeout) return CPATTN_ERR_TIMEOUT;
+  return (v & kStatusBounds) ? CPATTN_ERR_DEVICE_CHECK : CPATTN_OK;
 }
 
 cpattn_status cpattn_profile_begin(int capacity) {

@@ -596,6 +596,11 @@ __global__ void __launch_bounds__(PairLayout::kThreads, 1)
           (pd.mode == kAccInit || pd.mode == kAccMerge || pd.mode == kAccFinal))
         dep = p.dep_counters + pd.dep_base +
               ((int64_t)(kRowPair ? it.qt * 2 + (int)rank : it.qt) * p.Hq + head) * p.B + it.b;
+      if (kDebugChecks && dep != nullptr &&
+          (dep < p.dep_counters || dep >= p.dep_counters + p.n_dep_counters)) {
+        if (lane == 0) atomicOr(&g_attn_pair_status, kStatusBounds);
+        dep = nullptr;
+      }
       if (dep != nullptr && pd.visit > 0) {
         int got = 1;
         if (lane == 0) {
@@ -644,7 +649,7 @@ __global__ void __launch_bounds__(PairLayout::kThreads, 1)
       const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
       const float lse = l_tot > 0.f ? (m_fin + log2f(l_tot)) * 0.6931471805599453f : -INFINITY;
       RowSink sink;
-      if (valid) sink.init(p, pd, it.b, head, qrow, lse, par == 0, -1, &acc_lse_old);
+      if (valid) sink.init(p, pd, it.b, head, qrow, lse, par == 0, -1, &acc_lse_old, &g_attn_pair_status);
       // Warp par writes output columns [64 par, 64 par + 64).
 #pragma unroll 1
       for (int cc = 0; cc < 2; ++cc) {

@@ -21,6 +21,10 @@
 #include "epilogue.cuh"
 
 namespace cpattn {
+
+// Device status word of this kernel (debug-build bounds checks).
+__device__ unsigned int g_attn_simt_status;
+
 namespace {
 
 constexpr int kRows = 8;   // query rows per CTA (one per warp)
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(kRows * 32) attn_simt_kernel(const __grid_cons
 #pragma unroll
   for (int e = 0; e < E; ++e) o[e] *= inv;
   RowSink sink;
-  sink.init(p, pd, b, h, i, lse, lane == 0);
+  sink.init(p, pd, b, h, i, lse, lane == 0, -1, nullptr, &g_attn_simt_status);
   sink.put<E>(lane * E, o);
 }
 
@@ -160,6 +164,17 @@ cudaError_t launch_attn_simt(AttnParams &p, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+unsigned int attn_simt_read_status(bool clear, cudaError_t *err) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_attn_simt_status, sizeof(v));
+  if (e == cudaSuccess && clear) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_attn_simt_status, &zero, sizeof(zero));
+  }
+  if (err) *err = e;
+  return v;
 }
 
 }  // namespace cpattn

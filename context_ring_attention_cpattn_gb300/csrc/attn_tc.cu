@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(Layout::kThreads, 1)
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       RowSink sink;
-      if (valid) sink.init(p, pd, it.b, head, qrow, lse, true, pd.slot + it.split);
+      if (valid) sink.init(p, pd, it.b, head, qrow, lse, true, pd.slot + it.split, nullptr, &g_attn_tc_status);
 #pragma unroll 1
       for (int cc = 0; cc < kD / 32; ++cc) {
         float ov[32];
@@ -552,11 +552,8 @@ unsigned int attn_tc_read_status(bool clear, cudaError_t *err) {
     const unsigned int zero = 0;
     e = cudaMemcpyToSymbol(g_attn_tc_status, &zero, sizeof(zero));
   }
-  unsigned int w = 0;
-  cudaError_t e2 = cudaSuccess;
-  if (e == cudaSuccess) w = attn_pair_read_status(clear, &e2);
-  if (err) *err = e != cudaSuccess ? e : e2;
-  return v | w;
+  if (err) *err = e;
+  return v;
 }
 
 }  // namespace cpattn

@@ -12,6 +12,19 @@ namespace cpattn {
 
 constexpr int kMaxPairs = 64;  // pairs per launch = ranks per ring step (n_chunks <= 64)
 
+// Debug builds (-DCPATTN_DEBUG) check, in every kernel, each destination row,
+// workspace slot and progress counter against its extent before the write; a
+// failed check skips the write and sets kStatusBounds in the kernel's device
+// status word (cpattn_device_status -> CPATTN_ERR_DEVICE_CHECK).  No check
+// traps.
+#ifdef CPATTN_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+constexpr unsigned int kStatusTimeout = 1u;  // a bounded wait gave up
+constexpr unsigned int kStatusBounds = 2u;   // a debug-build bounds check failed
+
 // Where a pair's result goes (mirrors cpattn_role).
 enum PairMode : int32_t {
   kStore = CPATTN_ROLE_STORE,
@@ -83,6 +96,9 @@ struct AttnParams {
   // Bound of every kernel-side wait, in ns of global time (set by the
   // launcher from the launch's planned work; at least 2 s).
   uint64_t wait_ns;
+  // Extents for the debug-build bounds checks: workspace slots and rows per
+  // slot of `part`, and the number of progress counters.
+  int32_t n_part_slots, part_rows, n_dep_counters, pad2;
   OutView out;              // final output (absolute q rows)
   OutView acc;              // Pass-KV fp32 accumulator (absolute q rows)
   OutView part;             // Pass-Q slot 0 (chunk-relative rows)
@@ -96,7 +112,7 @@ struct AttnParams {
 struct MergeNParams {
   int32_t B, H, D, chunk_rows;
   int32_t n_items;
-  int32_t pad;
+  int32_t n_part_slots;  // slots of `part` (debug-build bounds checks)
   OutView out;
   OutView part;
   int64_t part_o_stride, part_lse_stride;
@@ -138,5 +154,7 @@ TcItemShape attn_tc_item_shape(const AttnParams &p);
 // attn_tc_read_status reads (and clears) both tensor-core kernels' words.
 unsigned int attn_tc_read_status(bool clear, cudaError_t *err);
 unsigned int attn_pair_read_status(bool clear, cudaError_t *err);
+unsigned int attn_simt_read_status(bool clear, cudaError_t *err);
+unsigned int merge_read_status(bool clear, cudaError_t *err);
 
 }  // namespace cpattn

@@ -123,12 +123,27 @@ struct RowSink {
   // write_lse: this thread writes the LSE (one thread per row and head).
   // acc_lse_old: the accumulator LSE read beforehand (acc_lse), or null to
   // read it here.
+  // status: the calling kernel's device status word (debug-build checks).
   __device__ __forceinline__ void init(const AttnParams &p, const PairDesc &pd, int b, int h,
                                        int rel_row, float lse_p, bool write_lse, int slot = -1,
-                                       const float *acc_lse_old = nullptr) {
+                                       const float *acc_lse_old = nullptr,
+                                       unsigned int *status = nullptr) {
     mode = pd.mode;
     if (slot < 0) slot = pd.slot;
     const int64_t abs_row = (int64_t)pd.q_row0 + rel_row;
+    if constexpr (kDebugChecks) {
+      bool in = b >= 0 && b < p.B && h >= 0 && h < p.Hq;
+      if (mode == kPartial)
+        in = in && slot >= 0 && slot < p.n_part_slots && rel_row >= 0 && rel_row < p.part_rows;
+      else
+        in = in && abs_row >= 0 && abs_row < p.q_rows_total;
+      if (!in) {
+        if (status != nullptr) atomicOr(status, kStatusBounds);
+        dst = nullptr;
+        acc = nullptr;
+        return;
+      }
+    }
     acc = nullptr;
     wa = 0.f;
     wb = 1.f;
@@ -168,6 +183,7 @@ struct RowSink {
   // Columns [c0, c0 + N) of the row; v holds the normalised partial O_p.
   template <int N>
   __device__ __forceinline__ void put(int c0, float (&v)[N]) const {
+    if (kDebugChecks && dst == nullptr) return;  // failed bounds check
     if (acc != nullptr) {
       float a[N];
       load_f32<N>(acc, c0, a);

@@ -21,6 +21,10 @@
 #include "epilogue.cuh"
 
 namespace cpattn {
+
+// Device status word of the merge kernels (debug-build bounds checks).
+__device__ unsigned int g_merge_status;
+
 namespace {
 
 constexpr int kWarps = 8;
@@ -104,6 +108,10 @@ __global__ void __launch_bounds__(kWarps * 32) mergen_kernel(const __grid_consta
   const int64_t n_rows = (int64_t)p.B * p.chunk_rows * p.H;
   const int64_t r0 = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * R;
   if (r0 >= n_rows) return;
+  if (kDebugChecks && count > 0 && (slot0 < 0 || slot0 + count > p.n_part_slots)) {
+    if ((threadIdx.x & 31) == 0) atomicOr(&g_merge_status, kStatusBounds);
+    return;
+  }
   const float *lse0[R];
   const float *o0[R];
   float m[R], sum[R], acc[R][E];
@@ -197,6 +205,10 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int count = p.item_count[item];
   const int slot0 = p.item_slot0[item];
   const int64_t r = blockIdx.x;  // the grid has one CTA per row
+  if (kDebugChecks && count > 0 && (slot0 < 0 || slot0 + count > p.n_part_slots)) {
+    if (threadIdx.x == 0) atomicOr(&g_merge_status, kStatusBounds);
+    return;
+  }
   const int h = (int)(r % p.H);
   const int64_t s = (r / p.H) % p.chunk_rows;
   const int b = (int)(r / ((int64_t)p.H * p.chunk_rows));
@@ -320,6 +332,17 @@ cudaError_t launch_merge_n(const MergeNParams &p, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+unsigned int merge_read_status(bool clear, cudaError_t *err) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_merge_status, sizeof(v));
+  if (e == cudaSuccess && clear) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_merge_status, &zero, sizeof(zero));
+  }
+  if (err) *err = e;
+  return v;
 }
 
 }  // namespace cpattn

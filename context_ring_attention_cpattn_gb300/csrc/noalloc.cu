@@ -12,8 +12,10 @@
 // The array is ordinary static device memory: every GPU on which this code
 // is loaded holds CPATTN_NOALLOC_SCRATCH_BYTES until the process exits.  In
 // host code its name is only a host-side stand-in, so its device address is
-// obtained once per device with cudaGetSymbolAddress (with that device
-// current) and passed on as the workspace pointer.
+// obtained with cudaGetSymbolAddress (with the device current) on the first
+// call in each CUDA context of a device, and passed on as the workspace
+// pointer.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -27,17 +29,45 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[CPATTN_NOALLOC_SCRATCH
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 void *g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set up on the
-// first call for that device).  nullptr on failure.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+// The driver's cuCtxGetCurrent, looked up once (no link-time dependency on
+// the driver library).
+CtxGetCurrentFn ctx_get_current_fn() {
+  static const CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetCurrentFn>(ptr);
+    return nullptr;
+  }();
+  return fn;
+}
+
+// Device address of the scratch array on the current device.  It is looked
+// up (cudaGetSymbolAddress, with the device current) on the first call in
+// each CUDA context of the device and cached for that context: after a
+// cudaDeviceReset the module is loaded again, the context changes and the
+// address is looked up again.  nullptr on failure.
 void *scratch_on_current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  if (get_ctx == nullptr) return nullptr;
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return nullptr;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (ctx == nullptr || g_scratch_ptr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
+    // (Also makes the device's primary context current if none was.)
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return nullptr;
     g_scratch_ptr[dev] = ptr;
+    g_scratch_ctx[dev] = ctx;
   }
   return g_scratch_ptr[dev];
 }

@@ -57,7 +57,8 @@ typedef enum {
   CPATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head_dim not 64/128) */
   CPATTN_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or too small */
   CPATTN_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
-  CPATTN_ERR_TIMEOUT = 5       /* a kernel-side bounded wait gave up (device status) */
+  CPATTN_ERR_TIMEOUT = 5,      /* a kernel-side bounded wait gave up (device status) */
+  CPATTN_ERR_DEVICE_CHECK = 6  /* debug builds: a kernel bounds check failed (device status) */
 } cpattn_status;
 
 typedef enum { CPATTN_BF16 = 0, CPATTN_FP32 = 1 } cpattn_dtype;
@@ -360,9 +361,10 @@ cpattn_status cpattn_prefill_host(const cpattn_tensor *q, const cpattn_tensor *k
  *   - Problems whose cpattn_prefill_workspace_size exceeds
  *     CPATTN_NOALLOC_SCRATCH_BYTES return CPATTN_ERR_UNSUPPORTED before
  *     anything is enqueued (e.g. Pass-KV fits sq * hq * b <= ~130K rows at d = 128).
- *   - The first call on a device looks up the buffer's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *   - The first call in each CUDA context of a device (the first call on
+ *     the device, and again after a cudaDeviceReset) looks up the buffer's
+ *     device address (cudaGetSymbolAddress) with that device current; make
+ *     that first call before any stream capture.
  *   - All calls share the one buffer and it keeps the previous call's
  *     contents; nothing in it has to start at zero.  Calls that overlap on
  *     the GPU (different streams, or different host threads without ordering)
@@ -379,9 +381,12 @@ cpattn_status cpattn_prefill_noalloc(const cpattn_tensor *q, const cpattn_tensor
 const char *cpattn_status_string(cpattn_status s);
 
 /*
- * cpattn_device_status -- read (and if `clear`, reset) the device status word
- * that kernels set when a bounded wait gives up.  Synchronises the device.
- * Returns CPATTN_OK, CPATTN_ERR_TIMEOUT or CPATTN_ERR_CUDA.
+ * cpattn_device_status -- read (and if `clear`, reset) the device status words
+ * that kernels set when a bounded wait gives up, or -- in a library built with
+ * -DCPATTN_DEBUG -- when a bounds check on a destination row, workspace slot
+ * or progress counter fails (the write is skipped; nothing traps).
+ * Synchronises the device.  Returns CPATTN_OK, CPATTN_ERR_TIMEOUT (takes
+ * precedence), CPATTN_ERR_DEVICE_CHECK or CPATTN_ERR_CUDA.
  */
 cpattn_status cpattn_device_status(int clear);
 

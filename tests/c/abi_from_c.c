@@ -67,5 +67,6 @@ int main(void) {
             (mode == CPATTN_PASS_KV || mode == CPATTN_PASS_Q),
         "schedule choice");
   CHECK(strncmp(cpattn_status_string(CPATTN_ERR_TIMEOUT), "CPATTN", 6) == 0, "status string");
+  CHECK(strncmp(cpattn_status_string(CPATTN_ERR_DEVICE_CHECK), "CPATTN", 6) == 0, "status string");
   return 0;
 }

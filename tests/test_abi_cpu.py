@@ -178,7 +178,7 @@ def test_auto_launch_mode(lib, shape, dtype, want):
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(7):
         assert lib.cpattn_status_string(code).decode().startswith("CPATTN")
 
 
