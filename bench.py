@@ -38,7 +38,8 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # DRAM bytes (read + write) per tensor FLOP of the prefill attention kernel
 # from one ncu capture, and the kernel source it was taken from; the
 # roofline's traffic is null whenever the source differs from the capture.
-TRAFFIC_RECORD = {"sha": None, "bytes_per_flop": None, "capture": None}
+TRAFFIC_RECORD = {"sha": "a8279b7a24914d17", "bytes_per_flop": 52.0e6 / 5.498e11,
+                  "capture": "profiles/attn_pair_32k_step.md"}
 
 
 def load_peaks():
@@ -487,6 +488,11 @@ def main():
     elapsed, per_mode, recs = time_modes(B, w, q, k, v, outs, wss, args.steps, args.warmup, world,
                                          modes, profile_cap=cap, launch=launch)
     clk = clocks.stop()
+    # A kernel-side wait that gave up leaves garbage output: such a run is no
+    # measurement.
+    dev_status = B.device_status(clear=True)
+    if dev_status != 0:
+        print(f"bench: device status {dev_status} after the timed region", file=sys.stderr)
     ms_step = elapsed / args.steps
     value = world * flops_step * args.steps / (elapsed * 1e-3) / 1e12
 
@@ -640,7 +646,7 @@ def main():
                 "data": "synthetic (seeded i.i.d. N(0,1) Q/K/V, bf16)", "config": cfg,
                 "roofline": roofline, "merge_roofline": merge_roofline, "decode": decode,
                 "cpu_baseline": cpu_baseline, "e2e": e2e,
-                "gpu_launches": len(recs), "clocks": clk}
+                "gpu_launches": len(recs), "device_status": dev_status, "clocks": clk}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -257,18 +257,17 @@ __global__ void __launch_bounds__(PairLayout::kThreads, 1)
         mbar_expect_tx(bar(L::b_qfull), L::q_bytes);
         const int head = it.h0 + (kRowPair ? 0 : (int)rank);
         const int qrow = it.pd->q_row0 + it.i0 + (kRowPair ? (int)rank * kRows : 0);
-        for (int half = 0; half < 2; ++half)
-          tma_load_4d(sb + L::q_off + half * L::q_box, &tm_q, bar(L::b_qfull), half * 64, head, qrow,
-                      it.b);
+        // Both 64-column halves of the tile in one copy (the map's third
+        // dimension is the half).
+        tma_load_5d(sb + L::q_off, &tm_q, bar(L::b_qfull), 0, qrow, 0, head, it.b);
         ++nq;
         auto load_k = [&](int j) -> bool {
           const int gj = g + j, st = gj % kStages;
           if (gj >= kStages && !wait(bar(L::b_kvempty + st), ((gj / kStages) - 1) & 1)) return false;
           mbar_expect_tx(bar(L::b_kfull + st), L::k_bytes);
           const int row = it.pd->kv_row0 + j * kKeys + (int)rank * 64;
-          for (int half = 0; half < 2; ++half)
-            tma_load_4d(sb + L::k_off + st * L::k_bytes + half * L::k_box, &tm_k,
-                        bar(L::b_kfull + st), half * 64, it.hk, row, it.b);
+          tma_load_5d(sb + L::k_off + st * L::k_bytes, &tm_k, bar(L::b_kfull + st), 0, row, 0, it.hk,
+                      it.b);
           ++nk[st];
           return true;
         };
@@ -713,6 +712,25 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+// [b, s, h, 128] bf16 view -> 5-D tensor map (d % 64, s, d / 64, h, b), box
+// 64 x box_s x 2 x 1 x 1: one copy brings both 64-column halves of box_s
+// rows, half 1 box_s * 128 bytes after half 0, each half in the 128-byte
+// swizzled row layout of a separate 64-column copy.
+bool make_map_halves(CUtensorMap *map, const void *base, int64_t B, int64_t S, int64_t H,
+                     int64_t sb, int64_t ss, int64_t sh, uint32_t box_s) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  if (B == 1) sb = S * ss > 0 ? S * ss : 8;  // unused extent: any legal stride
+  cuuint64_t dims[5] = {64, (cuuint64_t)S, 2, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[4] = {(cuuint64_t)ss * 2, 128, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
+  cuuint32_t box[5] = {64, box_s, 2, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // [b, s, h, d] bf16 view -> 4-D tensor map (d, h, s, b), box 64 x 1 x box_s x 1.
 bool make_map(CUtensorMap *map, const void *base, int64_t B, int64_t S, int64_t H, int64_t D,
               int64_t sb, int64_t ss, int64_t sh, uint32_t box_s) {
@@ -748,8 +766,8 @@ cudaError_t launch_pair_t(AttnParams &p, cudaStream_t stream) {
   }
   if (total == 0) return cudaSuccess;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.q, p.B, p.q_rows_total, p.Hq, kD, p.q_sb, p.q_ss, p.q_sh, kRows) ||
-      !make_map(&mk, p.k, p.B, p.kv_rows_total, p.Hkv, kD, p.k_sb, p.k_ss, p.k_sh, 64) ||
+  if (!make_map_halves(&mq, p.q, p.B, p.q_rows_total, p.Hq, p.q_sb, p.q_ss, p.q_sh, kRows) ||
+      !make_map_halves(&mk, p.k, p.B, p.kv_rows_total, p.Hkv, p.k_sb, p.k_ss, p.k_sh, 64) ||
       !make_map(&mv, p.v, p.B, p.kv_rows_total, p.Hkv, kD, p.v_sb, p.v_ss, p.v_sh, kKeys))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
