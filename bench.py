@@ -385,6 +385,19 @@ def seeds_of(args):
     return (args.seed, args.seed + 1, args.seed + 2)
 
 
+LAUNCH_NAMES = {0: "one launch per ring step", 1: "persistent CTAs per ring step",
+                2: "one persistent launch for all ring steps",
+                4: "one persistent launch for all ring steps, on-chip Pass-KV accumulator"}
+
+
+def launch_modes(B, w, q, k, modes, launch):
+    """The launch mode each schedule resolves to (AUTO depends on the schedule)."""
+    names = {B.PASS_KV: "pass_kv", B.PASS_Q: "pass_q"}
+    pre = "auto: " if launch == B.LAUNCH_AUTO else ""
+    return {names[m]: pre + LAUNCH_NAMES[B.launch_mode(q, k, w.n_chunks, m, w.q_base, w.causal,
+                                                        launch=launch)] for m in modes}
+
+
 def time_workload(B, name, steps, warmup, world, modes, launch, peaks):
     """ms per layer (median) of each schedule on a named workload, with its
     causal-effective TFLOP/s and fraction of the bf16 peaks."""
@@ -399,9 +412,7 @@ def time_workload(B, name, steps, warmup, world, modes, launch, peaks):
     names = {B.PASS_KV: "pass_kv", B.PASS_Q: "pass_q"}
     f = w.causal_flops()
     out = {"flops_per_layer": f, "steps": steps, "warmup": warmup,
-           "launch_mode": ["per step", "persistent per step", "single launch"][
-               B.launch_mode(q, k, w.n_chunks, modes[0], w.q_base, w.causal, launch=launch)],
-           "dtype": w.dtype}
+           "launch_mode": launch_modes(B, w, q, k, modes, launch), "dtype": w.dtype}
     for m in modes:
         ms = statistics.median(pm[m])
         tf = f / (ms * 1e-3) / 1e12
@@ -424,9 +435,10 @@ def main():
     ap.add_argument("--skip-1m", action="store_true", help="do not time the 1M-token layer")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-decode", action="store_true", help="do not time the decode leg")
-    ap.add_argument("--launch", type=int, default=None,
+    ap.add_argument("--launch", type=int, default=None, choices=[0, 1, 2, 3, 4],
                     help="ring launch mode: 0 per step, 1 persistent per step, 2 one launch, "
-                         "3 auto (the library default)")
+                         "3 auto (the library default), 4 one launch with an on-chip Pass-KV "
+                         "accumulator")
     ap.add_argument("--schedules", default="both", choices=["both", "kv", "q"],
                     help="ring schedules in one step (default: Pass-KV then Pass-Q)")
     ap.add_argument("--cpu-rows", type=int, default=2048,
@@ -541,11 +553,7 @@ def main():
     decode = None if args.skip_decode else time_decode(B, args.steps, hbm_peak, peak_src)
     cfg = {"workload": w.name, "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim,
            "seq_len": w.sq, "n_chunks": w.n_chunks, "causal": w.causal,
-           "launch_mode": ("auto: " if launch == B.LAUNCH_AUTO else "") +
-                          ["one launch per ring step", "persistent CTAs per ring step",
-                           "one persistent launch for all ring steps"][
-                              B.launch_mode(q, k, w.n_chunks, modes[0], w.q_base, w.causal,
-                                            launch=launch)],
+           "launch_mode": launch_modes(B, w, q, k, modes, launch),
            "step": " + ".join({"pass_kv": "Pass-KV prefill", "pass_q": "Pass-Q prefill"}[names[m]]
                                for m in modes) + " of one layer",
            "flops_per_layer": flops_layer, "ms_per_layer": ms_layer,

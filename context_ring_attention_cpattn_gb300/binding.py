@@ -38,7 +38,7 @@ class PrefillOptions(ctypes.Structure):
 
 
 ASSIGN_CONTIGUOUS, ASSIGN_ZIGZAG = 0, 1
-LAUNCH_PER_STEP, LAUNCH_PERSISTENT_STEP, LAUNCH_SINGLE, LAUNCH_AUTO = 0, 1, 2, 3
+LAUNCH_PER_STEP, LAUNCH_PERSISTENT_STEP, LAUNCH_SINGLE, LAUNCH_AUTO, LAUNCH_SINGLE_ONCHIP = 0, 1, 2, 3, 4
 
 
 def _opts(assignment: int, launch: int = LAUNCH_AUTO, hold_ordered_waits: bool = False):

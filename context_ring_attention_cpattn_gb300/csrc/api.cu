@@ -372,14 +372,17 @@ WsLayout ws_layout(const Plan &pl, int64_t B, int64_t sq, int64_t hq, int64_t d,
                    int launch_mode = CPATTN_LAUNCH_PER_STEP) {
   WsLayout w;
   size_t off = 0;
-  if (launch_mode == CPATTN_LAUNCH_SINGLE) {
+  const bool onchip = launch_mode == CPATTN_LAUNCH_SINGLE_ONCHIP && pl.mode == CPATTN_PASS_KV;
+  if (launch_mode == CPATTN_LAUNCH_SINGLE || launch_mode == CPATTN_LAUNCH_SINGLE_ONCHIP) {
     w.table = off;
     off = align256(off + pl.entries.size() * sizeof(PairDesc));
+  }
+  if (launch_mode == CPATTN_LAUNCH_SINGLE) {
     w.counters = off;
     w.n_counters = (size_t)pl.P * tiles_per_piece(pl) * hq * B;
     off = align256(off + w.n_counters * sizeof(int32_t));
   }
-  if (pl.mode == CPATTN_PASS_KV && pl.need_acc) {
+  if (pl.mode == CPATTN_PASS_KV && pl.need_acc && !onchip) {
     w.acc_o = off;
     off = align256(off + (size_t)B * sq * hq * d * 4);
     w.acc_lse = off;
@@ -425,6 +428,11 @@ int launch_mode_of(const cpattn_prefill_options *opts) {
   return opts ? opts->launch : CPATTN_LAUNCH_DEFAULT;
 }
 
+bool valid_launch(int l) {
+  return l == CPATTN_LAUNCH_PER_STEP || l == CPATTN_LAUNCH_PERSISTENT_STEP ||
+         l == CPATTN_LAUNCH_SINGLE || l == CPATTN_LAUNCH_AUTO || l == CPATTN_LAUNCH_SINGLE_ONCHIP;
+}
+
 // CPATTN_LAUNCH_AUTO: one persistent launch for all ring steps when work
 // items are short (mean visible 128-key tiles per 128-row query tile below
 // kAutoSingleTiles), where each CTA's start-up and write-out is a large share
@@ -444,7 +452,8 @@ int resolve_launch(int lmode, const Plan &pl, const cpattn_tensor *q, int64_t q_
     rows += (double)pl.Cq;
   }
   const double tiles = rows > 0.0 ? vis / rows / 128.0 : 0.0;
-  return tiles < kAutoSingleTiles ? CPATTN_LAUNCH_SINGLE : CPATTN_LAUNCH_PER_STEP;
+  if (tiles >= kAutoSingleTiles) return CPATTN_LAUNCH_PER_STEP;
+  return pl.mode == CPATTN_PASS_KV ? CPATTN_LAUNCH_SINGLE_ONCHIP : CPATTN_LAUNCH_SINGLE;
 }
 
 // Called (at enqueue time, on the host) once the work that finalises output
@@ -467,10 +476,10 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
       CPATTN_OK)
     return s;
   int lmode = launch_mode_of(opts);
-  if (lmode != CPATTN_LAUNCH_PER_STEP && lmode != CPATTN_LAUNCH_PERSISTENT_STEP &&
-      lmode != CPATTN_LAUNCH_SINGLE && lmode != CPATTN_LAUNCH_AUTO)
-    return CPATTN_ERR_INVALID_ARG;
+  if (!valid_launch(lmode)) return CPATTN_ERR_INVALID_ARG;
   lmode = resolve_launch(lmode, pl, q, q_base, causal);
+  const bool onchip = lmode == CPATTN_LAUNCH_SINGLE_ONCHIP && pl.mode == CPATTN_PASS_KV;
+  const bool single = lmode == CPATTN_LAUNCH_SINGLE || lmode == CPATTN_LAUNCH_SINGLE_ONCHIP;
   const WsLayout wl = ws_layout(pl, q->b, q->s, q->h, q->d, lmode);
   if (wl.total > 0) {
     if (workspace == nullptr || ws_bytes < wl.total) return CPATTN_ERR_WORKSPACE;
@@ -482,7 +491,7 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
   AttnParams p;
   fill_inputs(p, q, k, v, causal, scale);
   p.out = out_view(o, lse);
-  if (wl.acc_lse > 0 || (pl.mode == CPATTN_PASS_KV && pl.need_acc)) {
+  if (pl.mode == CPATTN_PASS_KV && pl.need_acc && !onchip) {
     p.acc.o = ws + wl.acc_o;
     p.acc.lse = reinterpret_cast<float *>(ws + wl.acc_lse);
     p.acc.sh = q->d;
@@ -532,11 +541,8 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
     for (const auto &it : items) out.push_back(it.pd);
   };
 
-  if (lmode == CPATTN_LAUNCH_SINGLE && attn_tc_supported(p)) {
+  if (single && attn_tc_supported(p)) {
     NvtxRange range("cpattn %s ring, one launch", mode_name(mode));
-    // One persistent launch for every ring step.  Work items keep the ring's
-    // launch order; a Pass-KV accumulator update waits (bounded) until the
-    // previous visit of the same rows has finished.
     std::vector<PairDesc> table;
     size_t e0 = 0;
     for (int l = 0; l < pl.n_launches; ++l) {
@@ -546,17 +552,54 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
       e0 = e1;
     }
     const TcItemShape sh = attn_tc_item_shape(p);
-    std::vector<int> visits(pl.P, 0);
+    const int per_tile = (int)(q->h / sh.heads) * (int)q->b;
     int total = 0;
     double vis = 0.0;
-    for (auto &pd : table) {
-      pd.n_qtiles = (pd.q_len + sh.rows - 1) / sh.rows;
-      pd.cta_begin = total;
-      total += pd.n_qtiles * (int)(q->h / sh.heads) * (int)q->b;
-      const int piece = (int)(pd.q_row0 / pl.Cq);
-      if (pd.mode == kAccInit || pd.mode == kAccMerge || pd.mode == kAccFinal)
-        pd.visit = visits[piece]++;
-      vis += visible_pairs(pd.delta, pd.q_len, 0, pd.kv_len, causal != 0);
+    for (const auto &pd : table) vis += visible_pairs(pd.delta, pd.q_len, 0, pd.kv_len, causal != 0);
+    if (onchip) {
+      // Each Q piece's pairs in ring order form one run of work items: a
+      // work item streams every visiting K/V piece through one on-chip
+      // accumulator and stores the result (segment x: visit = x, slot = the
+      // run's length).  Runs with the most work first.
+      std::vector<std::vector<PairDesc>> runs(pl.P);
+      std::vector<double> work(pl.P, 0.0);
+      for (const auto &pd : table) {
+        const int piece = (int)(pd.q_row0 / pl.Cq);
+        runs[piece].push_back(pd);
+        work[piece] += visible_pairs(pd.delta, pd.q_len, 0, pd.kv_len, causal != 0);
+      }
+      std::vector<int> order;
+      for (int i = 0; i < pl.P; ++i)
+        if (!runs[i].empty()) order.push_back(i);
+      std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return work[a] > work[b]; });
+      table.clear();
+      for (int i : order) {
+        const int n = (int)runs[i].size();
+        const int n_qtiles = (runs[i][0].q_len + sh.rows - 1) / sh.rows;
+        for (int x = 0; x < n; ++x) {
+          PairDesc pd = runs[i][x];
+          pd.mode = kStore;
+          pd.visit = x;
+          pd.slot = n;
+          pd.n_qtiles = n_qtiles;
+          pd.cta_begin = total;
+          table.push_back(pd);
+        }
+        total += n_qtiles * per_tile;
+      }
+    } else {
+      // Work items keep the ring's launch order; a Pass-KV accumulator
+      // update waits (bounded) until the previous visit of the same rows has
+      // finished.
+      std::vector<int> visits(pl.P, 0);
+      for (auto &pd : table) {
+        pd.n_qtiles = (pd.q_len + sh.rows - 1) / sh.rows;
+        pd.cta_begin = total;
+        total += pd.n_qtiles * per_tile;
+        const int piece = (int)(pd.q_row0 / pl.Cq);
+        if (pd.mode == kAccInit || pd.mode == kAccMerge || pd.mode == kAccFinal)
+          pd.visit = visits[piece]++;
+      }
     }
     // Inputs arriving piece by piece: the one launch reads all of them.
     for (int i = 0; i < pl.P && on_inputs != nullptr; ++i)
@@ -568,7 +611,8 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
       p.n_table = (int32_t)table.size();
       p.total_ctas = total;
       p.persistent_ctas = 1;
-      if (pl.mode == CPATTN_PASS_KV && pl.need_acc) {
+      p.seg_groups = onchip ? 1 : 0;
+      if (pl.mode == CPATTN_PASS_KV && pl.need_acc && !onchip) {
         p.dep_counters = reinterpret_cast<int32_t *>(ws + wl.counters);
         p.dep_hold = (opts != nullptr && opts->hold_ordered_waits != 0) ? (1 << 28) : 0;
         if (cudaMemsetAsync(p.dep_counters, 0, wl.n_counters * sizeof(int32_t), st) != cudaSuccess)
@@ -580,9 +624,10 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
       p.dep_counters = nullptr;
       p.dep_hold = 0;
       p.persistent_ctas = 0;
+      p.seg_groups = 0;
     }
   }
-  const bool per_step = !(lmode == CPATTN_LAUNCH_SINGLE && attn_tc_supported(p));
+  const bool per_step = !(single && attn_tc_supported(p));
   // Pass-Q merge of partials, and empty rows of chunks no key reaches: one
   // launch for the listed pieces.
   MergeNParams mp;
@@ -867,6 +912,7 @@ cpattn_status cpattn_prefill_workspace_size_ex(const cpattn_tensor *q, const cpa
     if ((s = build_plan(q->s, k->s, q_base, n_chunks, mode, causal, assignment_of(opts), pl)) !=
         CPATTN_OK)
       return s;
+    if (!valid_launch(launch_mode_of(opts))) return CPATTN_ERR_INVALID_ARG;
     const int lmode = resolve_launch(launch_mode_of(opts), pl, q, q_base, causal);
     *bytes = ws_layout(pl, q->b, q->s, q->h, q->d, lmode).total;
     return CPATTN_OK;
@@ -884,7 +930,7 @@ cpattn_status cpattn_prefill_launch_mode(const cpattn_tensor *q, const cpattn_te
     if (s != CPATTN_OK) return s;
     if ((s = check_view(k)) != CPATTN_OK) return s;
     const int lmode = launch_mode_of(opts);
-    if (lmode < CPATTN_LAUNCH_PER_STEP || lmode > CPATTN_LAUNCH_AUTO) return CPATTN_ERR_INVALID_ARG;
+    if (!valid_launch(lmode)) return CPATTN_ERR_INVALID_ARG;
     Plan pl;
     if ((s = build_plan(q->s, k->s, q_base, n_chunks, mode, causal, assignment_of(opts), pl)) !=
         CPATTN_OK)

@@ -132,7 +132,7 @@ constexpr uint32_t kIdescPV = make_idesc(2 * kRows, kD, true);
 
 static_assert(sizeof(AttnParams) + 3 * sizeof(CUtensorMap) <= 4096, "kernel parameters too large");
 
-template <bool kPersistent, bool kRowPair>
+template <bool kPersistent, bool kRowPair, bool kSegs>
 __global__ void __launch_bounds__(PairLayout::kThreads, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnParams p) {
@@ -202,9 +202,31 @@ __global__ void __launch_bounds__(PairLayout::kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::tmem_slot_off);
 
   // ---- work item geometry (every role of both CTAs decodes items identically)
+  // A work item's K/V steps are those of its segments, in order: one pair,
+  // or, when the table groups pairs (p.seg_groups), every pair of one query
+  // piece in ring order, whose K/V pieces then stream through one on-chip
+  // accumulator.  In a group, segment x carries visit = x and slot = the
+  // group's size, and all share cta_begin.
+  struct Seg {
+    int n_kv, n_unmasked;
+  };
+  // 128-key steps of segment `sp` for query rows i0 .. i0 + q_rows - 1 of its
+  // piece: keys [0, kv_end) are visible to some row, [0, full_end) to all.
+  auto seg_steps = [&](const PairDesc &sp, int i0, int q_rows) -> Seg {
+    int64_t kv_end = sp.kv_len, full_end = sp.kv_len;
+    if (p.causal) {
+      const int64_t last_lim = (int64_t)(i0 + q_rows - 1) + sp.delta + 1;
+      const int64_t first_lim = (int64_t)i0 + sp.delta + 1;
+      kv_end = last_lim < kv_end ? last_lim : kv_end;
+      full_end = first_lim < full_end ? first_lim : full_end;
+    }
+    if (kv_end < 0) kv_end = 0;
+    if (full_end < 0) full_end = 0;
+    return {(int)((kv_end + kKeys - 1) / kKeys), (int)(full_end / kKeys)};
+  };
   struct Item {
-    const PairDesc *pd;
-    int h0, hk, i0, q_rows, qt, b, n_kv, n_unmasked;
+    const PairDesc *pd;  // first segment
+    int n_segs, h0, hk, i0, q_rows, qt, b, n_kv, n_unmasked;  // n_unmasked: one-pair items
   };
   auto decode = [&](int item, Item &it) {
     int lo = 0, hi = n_pairs - 1;  // last pair whose cta_begin <= item
@@ -212,8 +234,10 @@ __global__ void __launch_bounds__(PairLayout::kThreads, 1)
       const int mid = (lo + hi + 1) >> 1;
       if (pairs[mid].cta_begin <= item) lo = mid; else hi = mid - 1;
     }
+    if constexpr (kSegs) lo -= pairs[lo].visit;
     const PairDesc &pd = pairs[lo];
     it.pd = &pd;
+    it.n_segs = kSegs ? pd.slot : 1;
     int local = item - pd.cta_begin;
     constexpr int hpi = kRowPair ? 1 : 2, rpi = kRowPair ? 2 * kRows : kRows;
     const int n_hg = p.Hq / hpi;
@@ -225,18 +249,49 @@ __global__ void __launch_bounds__(PairLayout::kThreads, 1)
     it.hk = it.h0 / (p.Hq / p.Hkv);
     it.i0 = it.qt * rpi;
     it.q_rows = min(rpi, pd.q_len - it.i0);
-    // Keys [0, kv_end) are visible to some row of the item; [0, full_end) to every row.
-    int64_t kv_end = pd.kv_len, full_end = pd.kv_len;
-    if (p.causal) {
-      const int64_t last_lim = (int64_t)(it.i0 + it.q_rows - 1) + pd.delta + 1;
-      const int64_t first_lim = (int64_t)it.i0 + pd.delta + 1;
-      kv_end = last_lim < kv_end ? last_lim : kv_end;
-      full_end = first_lim < full_end ? first_lim : full_end;
+    if constexpr (kSegs) {
+      it.n_kv = 0;
+      for (int x = 0; x < it.n_segs; ++x) it.n_kv += seg_steps(it.pd[x], it.i0, it.q_rows).n_kv;
+      it.n_unmasked = 0;
+    } else {
+      const Seg q = seg_steps(pd, it.i0, it.q_rows);
+      it.n_kv = q.n_kv;
+      it.n_unmasked = q.n_unmasked;
     }
-    if (kv_end < 0) kv_end = 0;
-    if (full_end < 0) full_end = 0;
-    it.n_kv = (int)((kv_end + kKeys - 1) / kKeys);
-    it.n_unmasked = (int)(full_end / kKeys);
+  };
+  // Position in an item's step sequence: segment, step within it.
+  struct Cursor {
+    const PairDesc *sp;
+    int left, js, n_kv, n_unmasked;
+  };
+  auto cursor_at = [&](const Item &it, int j) -> Cursor {
+    Cursor c;
+    c.sp = it.pd;
+    c.left = it.n_segs;
+    c.js = j;
+    Seg q = seg_steps(*c.sp, it.i0, it.q_rows);
+    c.n_kv = q.n_kv;
+    c.n_unmasked = q.n_unmasked;
+    while (c.js >= c.n_kv && c.left > 1) {
+      c.js -= c.n_kv;
+      ++c.sp;
+      --c.left;
+      q = seg_steps(*c.sp, it.i0, it.q_rows);
+      c.n_kv = q.n_kv;
+      c.n_unmasked = q.n_unmasked;
+    }
+    return c;
+  };
+  auto cursor_advance = [&](const Item &it, Cursor &c, int by) {
+    c.js += by;
+    while (c.js >= c.n_kv && c.left > 1) {
+      c.js -= c.n_kv;
+      ++c.sp;
+      --c.left;
+      const Seg q = seg_steps(*c.sp, it.i0, it.q_rows);
+      c.n_kv = q.n_kv;
+      c.n_unmasked = q.n_unmasked;
+    }
   };
 
   if (warp == L::kTmaWarp) {
@@ -261,11 +316,24 @@ __global__ void __launch_bounds__(PairLayout::kThreads, 1)
         // dimension is the half).
         tma_load_5d(sb + L::q_off, &tm_q, bar(L::b_qfull), 0, qrow, 0, head, it.b);
         ++nq;
+        // K/V rows of step j: a one-pair item indexes its pair; an item of
+        // grouped pairs walks them with cursors (K runs one step ahead of V).
+        [[maybe_unused]] Cursor ck, cv;
+        if constexpr (kSegs) ck = cv = cursor_at(it, 0);
+        auto tile_row = [&](Cursor &c, int j) -> int {
+          if constexpr (kSegs) {
+            const int row = c.sp->kv_row0 + c.js * kKeys;
+            cursor_advance(it, c, 1);
+            return row;
+          } else {
+            return it.pd->kv_row0 + j * kKeys;
+          }
+        };
         auto load_k = [&](int j) -> bool {
           const int gj = g + j, st = gj % kStages;
           if (gj >= kStages && !wait(bar(L::b_kvempty + st), ((gj / kStages) - 1) & 1)) return false;
           mbar_expect_tx(bar(L::b_kfull + st), L::k_bytes);
-          const int row = it.pd->kv_row0 + j * kKeys + (int)rank * 64;
+          const int row = tile_row(ck, j) + (int)rank * 64;
           tma_load_5d(sb + L::k_off + st * L::k_bytes, &tm_k, bar(L::b_kfull + st), 0, row, 0, it.hk,
                       it.b);
           ++nk[st];
@@ -278,7 +346,7 @@ __global__ void __launch_bounds__(PairLayout::kThreads, 1)
           if (gj >= kStages && !wait(bar(L::b_kvempty + st), ((gj / kStages) - 1) & 1)) return false;
           mbar_expect_tx(bar(L::b_vfull + st), L::v_bytes);
           tma_load_4d(sb + L::v_off + st * L::v_bytes, &tm_v, bar(L::b_vfull + st), (int)rank * 64,
-                      it.hk, it.pd->kv_row0 + j * kKeys, it.b);
+                      it.hk, tile_row(cv, j), it.b);
           ++nv[st];
           return true;
         };
@@ -457,13 +525,43 @@ __global__ void __launch_bounds__(PairLayout::kThreads, 1)
       const int qrow = it.i0 + trow;                           // row within the pair's chunk
       const int head = it.h0 + (kRowPair ? 0 : (int)rank);
       const bool valid = trow < it.q_rows;
-      int64_t lim = pd.kv_len;  // this row's visible keys: [0, lim)
-      if (p.causal) {
-        const int64_t c = (int64_t)qrow + pd.delta + 1;
-        lim = c < lim ? c : lim;
-      }
       float m_own = -INFINITY, l_run = 0.f;  // this warp's row sum and its reference
+      // The segment of this warp's next step (persistent launches, whose
+      // items may span several pairs); one-pair items use pd directly.
+      // Masking of item-local step j: it is partly masked when j >= unm_at,
+      // and then this row sees the keys before lim_at - 128 j.  An item of
+      // grouped pairs moves both to the segment of step j as it goes.
+      int64_t lim_at = pd.kv_len;
+      int unm_at = it.n_unmasked;
+      if constexpr (!kSegs) {
+        if (p.causal) {
+          const int64_t c = (int64_t)qrow + pd.delta + 1;
+          lim_at = c < lim_at ? c : lim_at;
+        }
+      }
+      [[maybe_unused]] int seg_end = 0;
+      [[maybe_unused]] const PairDesc *segp = &pd;
+      [[maybe_unused]] int seg_left = it.n_segs;
+      [[maybe_unused]] auto enter_seg = [&](int base) {
+        const Seg q = seg_steps(*segp, it.i0, it.q_rows);
+        int64_t lm = segp->kv_len;
+        if (p.causal) {
+          const int64_t c = (int64_t)qrow + segp->delta + 1;
+          lm = c < lm ? c : lm;
+        }
+        lim_at = lm + (int64_t)base * kKeys;
+        unm_at = base + q.n_unmasked;
+        seg_end = base + q.n_kv;
+      };
+      if constexpr (kSegs) enter_seg(0);
       for (int j = (par - g) & 1; j < n_kv; j += 2) {
+        if constexpr (kSegs) {
+          while (j >= seg_end && seg_left > 1) {
+            ++segp;
+            --seg_left;
+            enter_seg(seg_end);
+          }
+        }
         const int gj = g + j;
         // Warp-uniform outcome: the TMEM accesses below are warp-collective.
         if (!__all_sync(0xffffffffu, wait(bar(L::b_sfull + par), (gj >> 1) & 1))) {
@@ -482,8 +580,8 @@ __global__ void __launch_bounds__(PairLayout::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(lead_bar(L::b_sfree + par));
-        if (j >= it.n_unmasked) {
-          const int64_t nv = lim - (int64_t)j * kKeys;
+        if (j >= unm_at) {
+          const int64_t nv = lim_at - (int64_t)j * kKeys;
           const int nvis = nv < 0 ? 0 : (nv > kKeys ? kKeys : (int)nv);
 #pragma unroll
           for (int c = 0; c < kKeys; ++c)
@@ -747,10 +845,10 @@ bool make_map(CUtensorMap *map, const void *base, int64_t B, int64_t S, int64_t 
   return r == CUDA_SUCCESS;
 }
 
-template <bool kPersistent, bool kRowPair>
+template <bool kPersistent, bool kRowPair, bool kSegs = false>
 cudaError_t launch_pair_t(AttnParams &p, cudaStream_t stream) {
   using L = PairLayout;
-  auto kernel = attn_pair_kernel<kPersistent, kRowPair>;
+  auto kernel = attn_pair_kernel<kPersistent, kRowPair, kSegs>;
   int total = 0;
   if (p.pair_table != nullptr) {
     total = p.total_ctas;  // device-resident table: the caller set cta_begin / n_qtiles
@@ -825,6 +923,13 @@ cudaError_t launch_pair_t(AttnParams &p, cudaStream_t stream) {
 
 cudaError_t launch_pair_any(AttnParams &p, cudaStream_t stream) {
   const bool pers = p.persistent_ctas > 0;
+  if (p.seg_groups) {
+    // Grouped pairs (on-chip accumulation across a query piece's K/V pieces):
+    // persistent launches only, in their own kernel instance.
+    if (!pers || p.pair_table == nullptr) return cudaErrorInvalidValue;
+    return p.row_pair ? launch_pair_t<true, true, true>(p, stream)
+                      : launch_pair_t<true, false, true>(p, stream);
+  }
   if (p.row_pair)
     return pers ? launch_pair_t<true, true>(p, stream) : launch_pair_t<false, true>(p, stream);
   return pers ? launch_pair_t<true, false>(p, stream) : launch_pair_t<false, false>(p, stream);

@@ -98,7 +98,10 @@ struct AttnParams {
   uint64_t wait_ns;
   // Extents for the debug-build bounds checks: workspace slots and rows per
   // slot of `part`, and the number of progress counters.
-  int32_t n_part_slots, part_rows, n_dep_counters, pad2;
+  int32_t n_part_slots, part_rows, n_dep_counters;
+  // Nonzero: pair_table groups the pairs of each query piece (ring order)
+  // into one run of work items that accumulates on chip (attn_pair only).
+  int32_t seg_groups;
   OutView out;              // final output (absolute q rows)
   OutView acc;              // Pass-KV fp32 accumulator (absolute q rows)
   OutView part;             // Pass-Q slot 0 (chunk-relative rows)

@@ -226,11 +226,19 @@ typedef enum { CPATTN_ASSIGN_CONTIGUOUS = 0, CPATTN_ASSIGN_ZIGZAG = 1 } cpattn_a
  *                        waits -- bounded, CPATTN_ERR_TIMEOUT if it gives up --
  *                        until the previous step's update of the same rows has
  *                        finished.  Launched cooperatively (all CTAs resident).
- *   AUTO                 SINGLE when the tensor-core kernel applies (bf16,
- *                        head_dim 128) and the ring's work items are short --
- *                        fewer than 48 visible 128-key tiles per 128-row
- *                        query tile on average, where a CTA's fixed start-up
- *                        and write-out cost is a large share of its work --
+ *   SINGLE_ONCHIP        one persistent launch for all ring steps; Pass-KV
+ *                        keeps each query tile's accumulator on chip (TMEM)
+ *                        while the visiting K/V pieces stream through it in
+ *                        ring order, and writes O and LSE once (no fp32
+ *                        accumulator in the workspace, no ordered waits).
+ *                        Pass-Q runs as SINGLE.  Tensor-core kernel only
+ *                        (bf16, head_dim 128); otherwise PER_STEP.
+ *   AUTO                 when the tensor-core kernel applies (bf16, head_dim
+ *                        128) and the ring's work items are short -- fewer
+ *                        than 48 visible 128-key tiles per 128-row query tile
+ *                        on average, where a CTA's fixed start-up and
+ *                        write-out cost is a large share of its work --
+ *                        SINGLE_ONCHIP for Pass-KV and SINGLE for Pass-Q;
  *                        else PER_STEP.
  * CPATTN_LAUNCH_DEFAULT (options NULL or launch = DEFAULT) is AUTO.
  */
@@ -239,7 +247,8 @@ typedef enum {
   CPATTN_LAUNCH_PERSISTENT_STEP = 1,
   CPATTN_LAUNCH_SINGLE = 2,
   CPATTN_LAUNCH_AUTO = 3,
-  CPATTN_LAUNCH_DEFAULT = 3
+  CPATTN_LAUNCH_DEFAULT = 3,
+  CPATTN_LAUNCH_SINGLE_ONCHIP = 4
 } cpattn_launch_mode;
 
 /*
@@ -259,8 +268,9 @@ typedef struct {
 
 /*
  * cpattn_prefill_launch_mode -- the launch mode cpattn_prefill_ex would use
- * for these shapes and options (CPATTN_LAUNCH_AUTO resolved to PER_STEP or
- * SINGLE; an explicit mode is returned as given).  Host only, no CUDA call.
+ * for these shapes and options (CPATTN_LAUNCH_AUTO resolved to PER_STEP,
+ * SINGLE or SINGLE_ONCHIP; an explicit mode is returned as given).  Host
+ * only, no CUDA call.
  */
 cpattn_status cpattn_prefill_launch_mode(const cpattn_tensor *q, const cpattn_tensor *k,
                                          int64_t q_base, int n_chunks, int mode, int causal,

@@ -56,7 +56,10 @@ int main(void) {
   int launch = -1;
   CHECK(cpattn_prefill_launch_mode(&q, &k, 0, 8, CPATTN_PASS_KV, 1, NULL, &launch) == CPATTN_OK,
         "launch mode status");
-  CHECK(launch == CPATTN_LAUNCH_SINGLE, "short work items take one launch");
+  CHECK(launch == CPATTN_LAUNCH_SINGLE_ONCHIP, "short Pass-KV items take one on-chip launch");
+  CHECK(cpattn_prefill_launch_mode(&q, &k, 0, 8, CPATTN_PASS_Q, 1, NULL, &launch) == CPATTN_OK,
+        "launch mode status");
+  CHECK(launch == CPATTN_LAUNCH_SINGLE, "short Pass-Q items take one launch");
 
   size_t ws = 0;
   CHECK(cpattn_prefill_workspace_size(&q, &k, 0, 8, CPATTN_PASS_Q, 1, &ws) == CPATTN_OK && ws > 0,

@@ -68,13 +68,14 @@ static void sweep_plans(void) {
             EXPECT(critical >= 0.0 && total >= critical - 1e-9, "critical path values");
             cpattn_tensor q = view(2, s, 4, 128, CPATTN_BF16), k = view(2, s, 2, 128, CPATTN_BF16);
             size_t ws = 0;
-            for (int lm = CPATTN_LAUNCH_PER_STEP; lm <= CPATTN_LAUNCH_AUTO; ++lm) {
+            for (int lm = CPATTN_LAUNCH_PER_STEP; lm <= CPATTN_LAUNCH_SINGLE_ONCHIP; ++lm) {
               o.launch = lm;
               EXPECT(cpattn_prefill_workspace_size_ex(&q, &k, bases[bi], n, mode, causal, &o, &ws) ==
                          CPATTN_OK, "workspace size");
               int launch = -1;
               EXPECT(cpattn_prefill_launch_mode(&q, &k, bases[bi], n, mode, causal, &o, &launch) ==
-                         CPATTN_OK && launch >= 0 && launch <= CPATTN_LAUNCH_SINGLE,
+                         CPATTN_OK && launch >= 0 && launch != CPATTN_LAUNCH_AUTO &&
+                         launch <= CPATTN_LAUNCH_SINGLE_ONCHIP,
                      "launch mode");
             }
             int pick = 0;

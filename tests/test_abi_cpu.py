@@ -146,28 +146,29 @@ def test_workspace_sizes(lib):
     assert size.value == align(slots * per_slot_o) + align(slots * per_slot_l)
 
 
-@pytest.mark.parametrize("shape,dtype,want", [
-    ((8192, 8192, 32, 8, 8), B.BF16, B.LAUNCH_SINGLE),        # 8-tile work items
-    ((2048, 32768, 16, 1, 8), B.BF16, B.LAUNCH_SINGLE),       # partial prefill, 32-tile items
-    ((131072, 131072, 16, 1, 16), B.BF16, B.LAUNCH_PER_STEP),  # ~60-tile items
-    ((8192, 8192, 32, 8, 8), B.FP32, B.LAUNCH_PER_STEP),      # no tensor-core kernel
+@pytest.mark.parametrize("shape,dtype,want_kv,want_q", [
+    ((8192, 8192, 32, 8, 8), B.BF16, B.LAUNCH_SINGLE_ONCHIP, B.LAUNCH_SINGLE),   # 8-tile items
+    ((2048, 32768, 16, 1, 8), B.BF16, B.LAUNCH_SINGLE_ONCHIP, B.LAUNCH_SINGLE),  # 32-tile items
+    ((131072, 131072, 16, 1, 16), B.BF16, B.LAUNCH_PER_STEP, B.LAUNCH_PER_STEP),  # ~60-tile
+    ((8192, 8192, 32, 8, 8), B.FP32, B.LAUNCH_PER_STEP, B.LAUNCH_PER_STEP),      # no tensor cores
 ])
-def test_auto_launch_mode(lib, shape, dtype, want):
+def test_auto_launch_mode(lib, shape, dtype, want_kv, want_q):
     """CPATTN_LAUNCH_AUTO (the default) resolves to one launch for all ring
-    steps when work items are short, one launch per step otherwise; the
-    default workspace size is the resolved mode's."""
+    steps when work items are short (Pass-KV with its accumulator on chip),
+    one launch per step otherwise; the default workspace size is the
+    resolved mode's."""
     sq, skv, hq, hkv, n = shape
     q_base = skv - sq
     q, k = T(dtype=dtype, s=sq, h=hq), T(dtype=dtype, s=skv, h=hkv)
-    got = ctypes.c_int(-1)
-    assert lib.cpattn_prefill_launch_mode(ctypes.byref(q), ctypes.byref(k), q_base, n, 1, 1, None,
-                                          ctypes.byref(got)) == 0
-    assert got.value == want
-    explicit = ctypes.byref(B.PrefillOptions(0, B.LAUNCH_PERSISTENT_STEP))
-    assert lib.cpattn_prefill_launch_mode(ctypes.byref(q), ctypes.byref(k), q_base, n, 1, 1, explicit,
-                                          ctypes.byref(got)) == 0
-    assert got.value == B.LAUNCH_PERSISTENT_STEP
-    for mode in (1, 2):
+    for mode, want in ((1, want_kv), (2, want_q)):
+        got = ctypes.c_int(-1)
+        assert lib.cpattn_prefill_launch_mode(ctypes.byref(q), ctypes.byref(k), q_base, n, mode, 1,
+                                              None, ctypes.byref(got)) == 0
+        assert got.value == want
+        explicit = ctypes.byref(B.PrefillOptions(0, B.LAUNCH_PERSISTENT_STEP))
+        assert lib.cpattn_prefill_launch_mode(ctypes.byref(q), ctypes.byref(k), q_base, n, mode, 1,
+                                              explicit, ctypes.byref(got)) == 0
+        assert got.value == B.LAUNCH_PERSISTENT_STEP
         a, b = ctypes.c_size_t(), ctypes.c_size_t()
         assert lib.cpattn_prefill_workspace_size(ctypes.byref(q), ctypes.byref(k), q_base, n, mode, 1,
                                                  ctypes.byref(a)) == 0
@@ -175,6 +176,29 @@ def test_auto_launch_mode(lib, shape, dtype, want):
         assert lib.cpattn_prefill_workspace_size_ex(ctypes.byref(q), ctypes.byref(k), q_base, n,
                                                     mode, 1, resolved, ctypes.byref(b)) == 0
         assert a.value == b.value
+
+
+def test_onchip_workspace_has_no_accumulator(lib):
+    """SINGLE_ONCHIP Pass-KV keeps the accumulator on chip: its workspace is
+    the pair table alone, SINGLE's adds progress counters and the fp32
+    accumulator (O and LSE); an unknown launch mode is an argument error."""
+    sq, hq, hkv, n = 8192, 32, 8, 8
+    q, k = T(dtype=B.BF16, s=sq, h=hq), T(dtype=B.BF16, s=sq, h=hkv)
+    sizes = {}
+    for launch in (B.LAUNCH_SINGLE, B.LAUNCH_SINGLE_ONCHIP):
+        size = ctypes.c_size_t()
+        assert lib.cpattn_prefill_workspace_size_ex(ctypes.byref(q), ctypes.byref(k), 0, n, 1, 1,
+                                                    ctypes.byref(B.PrefillOptions(0, launch)),
+                                                    ctypes.byref(size)) == 0
+        sizes[launch] = size.value
+    align = lambda x: (x + 255) // 256 * 256
+    acc = align(sq * hq * 128 * 4) + align(hq * sq * 4)
+    assert sizes[B.LAUNCH_SINGLE] - sizes[B.LAUNCH_SINGLE_ONCHIP] >= acc
+    assert sizes[B.LAUNCH_SINGLE_ONCHIP] < 64 * 1024
+    size = ctypes.c_size_t()
+    assert lib.cpattn_prefill_workspace_size_ex(ctypes.byref(q), ctypes.byref(k), 0, n, 1, 1,
+                                                ctypes.byref(B.PrefillOptions(0, 7)),
+                                                ctypes.byref(size)) == 1
 
 
 def test_status_strings(lib):
