@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # DRAM bytes (read + write) per tensor FLOP of the prefill attention kernel
 # from one ncu capture, and the kernel source it was taken from; the
 # roofline's traffic is null whenever the source differs from the capture.
-TRAFFIC_RECORD = {"sha": "a8279b7a24914d17", "bytes_per_flop": 52.0e6 / 5.498e11,
+TRAFFIC_RECORD = {"sha": "4247d6041a1fae0a", "bytes_per_flop": 52.07e6 / 5.498e11,
                   "capture": "profiles/attn_pair_32k_step.md"}
 
 
