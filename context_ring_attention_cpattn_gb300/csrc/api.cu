@@ -440,9 +440,15 @@ bool valid_launch(int l) {
 // per step vs single): 8-tile items 589 vs 687, 32-tile 922 vs 1036,
 // 60-tile 1367 vs 1304.
 constexpr double kAutoSingleTiles = 48.0;
+// K/V bytes up to which an on-chip Pass-KV launch keeps its K/V reads in L2
+// (the GPU has 126 MB).
+constexpr double kOnchipKvBytes = 96.0 * 1024 * 1024;
 
-int resolve_launch(int lmode, const Plan &pl, const cpattn_tensor *q, int64_t q_base,
-                   int causal) {
+// pipelined_io: the call overlaps host copies with the ring (the host-buffer
+// entry point), which one launch for all steps cannot do; it then keeps one
+// launch per step wherever items are long.
+int resolve_launch(int lmode, const Plan &pl, const cpattn_tensor *q, const cpattn_tensor *k,
+                   int64_t q_base, int causal, bool pipelined_io = false) {
   if (lmode != CPATTN_LAUNCH_AUTO) return lmode;
   if (q->dtype != CPATTN_BF16 || q->d != 128) return CPATTN_LAUNCH_PER_STEP;  // no tensor-core kernel
   double vis = 0.0, rows = 0.0;
@@ -452,8 +458,19 @@ int resolve_launch(int lmode, const Plan &pl, const cpattn_tensor *q, int64_t q_
     rows += (double)pl.Cq;
   }
   const double tiles = rows > 0.0 ? vis / rows / 128.0 : 0.0;
-  if (tiles >= kAutoSingleTiles) return CPATTN_LAUNCH_PER_STEP;
-  return pl.mode == CPATTN_PASS_KV ? CPATTN_LAUNCH_SINGLE_ONCHIP : CPATTN_LAUNCH_SINGLE;
+  const bool short_items = tiles < kAutoSingleTiles;
+  if (pl.mode == CPATTN_PASS_KV) {
+    // The accumulator on chip (no fp32 round trip per visit) when items are
+    // short or K and V stay in L2: an on-chip item streams its own sequence
+    // of K/V pieces, so concurrent items read different pieces, which L2 can
+    // hold only for a small K/V.  Measured on one GB300: 128K (K/V 64 MiB)
+    // 44.5 vs 49.6 ms per layer per step; 1M (K/V 512 MiB) 1718 vs 1362 ms.
+    const double kv_bytes = (double)k->b * (double)k->s * (double)k->h * (double)k->d * 2.0 * 2.0;
+    return (short_items || (!pipelined_io && kv_bytes <= kOnchipKvBytes))
+               ? CPATTN_LAUNCH_SINGLE_ONCHIP
+               : CPATTN_LAUNCH_PER_STEP;
+  }
+  return short_items ? CPATTN_LAUNCH_SINGLE : CPATTN_LAUNCH_PER_STEP;
 }
 
 // Called (at enqueue time, on the host) once the work that finalises output
@@ -477,7 +494,7 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
     return s;
   int lmode = launch_mode_of(opts);
   if (!valid_launch(lmode)) return CPATTN_ERR_INVALID_ARG;
-  lmode = resolve_launch(lmode, pl, q, q_base, causal);
+  lmode = resolve_launch(lmode, pl, q, k, q_base, causal, on_final != nullptr || on_inputs != nullptr);
   const bool onchip = lmode == CPATTN_LAUNCH_SINGLE_ONCHIP && pl.mode == CPATTN_PASS_KV;
   const bool single = lmode == CPATTN_LAUNCH_SINGLE || lmode == CPATTN_LAUNCH_SINGLE_ONCHIP;
   const WsLayout wl = ws_layout(pl, q->b, q->s, q->h, q->d, lmode);
@@ -900,9 +917,10 @@ cpattn_status cpattn_prefill_workspace_size(const cpattn_tensor *q, const cpattn
   return cpattn_prefill_workspace_size_ex(q, k, q_base, n_chunks, mode, causal, nullptr, bytes);
 }
 
-cpattn_status cpattn_prefill_workspace_size_ex(const cpattn_tensor *q, const cpattn_tensor *k,
-                                               int64_t q_base, int n_chunks, int mode, int causal,
-                                               const cpattn_prefill_options *opts, size_t *bytes) {
+static cpattn_status prefill_ws_bytes(const cpattn_tensor *q, const cpattn_tensor *k, int64_t q_base,
+                               int n_chunks, int mode, int causal,
+                               const cpattn_prefill_options *opts, bool pipelined_io,
+                               size_t *bytes) {
   try {
     if (bytes == nullptr) return CPATTN_ERR_INVALID_ARG;
     cpattn_status s = check_view(q);
@@ -913,12 +931,18 @@ cpattn_status cpattn_prefill_workspace_size_ex(const cpattn_tensor *q, const cpa
         CPATTN_OK)
       return s;
     if (!valid_launch(launch_mode_of(opts))) return CPATTN_ERR_INVALID_ARG;
-    const int lmode = resolve_launch(launch_mode_of(opts), pl, q, q_base, causal);
+    const int lmode = resolve_launch(launch_mode_of(opts), pl, q, k, q_base, causal, pipelined_io);
     *bytes = ws_layout(pl, q->b, q->s, q->h, q->d, lmode).total;
     return CPATTN_OK;
   } catch (...) {
     return CPATTN_ERR_INVALID_ARG;
   }
+}
+
+cpattn_status cpattn_prefill_workspace_size_ex(const cpattn_tensor *q, const cpattn_tensor *k,
+                                               int64_t q_base, int n_chunks, int mode, int causal,
+                                               const cpattn_prefill_options *opts, size_t *bytes) {
+  return prefill_ws_bytes(q, k, q_base, n_chunks, mode, causal, opts, false, bytes);
 }
 
 cpattn_status cpattn_prefill_launch_mode(const cpattn_tensor *q, const cpattn_tensor *k,
@@ -935,7 +959,7 @@ cpattn_status cpattn_prefill_launch_mode(const cpattn_tensor *q, const cpattn_te
     if ((s = build_plan(q->s, k->s, q_base, n_chunks, mode, causal, assignment_of(opts), pl)) !=
         CPATTN_OK)
       return s;
-    *launch = resolve_launch(lmode, pl, q, q_base, causal);
+    *launch = resolve_launch(lmode, pl, q, k, q_base, causal);
     return CPATTN_OK;
   } catch (...) {
     return CPATTN_ERR_INVALID_ARG;
@@ -1183,7 +1207,7 @@ cpattn_status cpattn_prefill_host_scratch_size(const cpattn_tensor *q, const cpa
                                                int out_dtype, size_t *bytes) {
   if (bytes == nullptr || elem_bytes(out_dtype) == 0) return CPATTN_ERR_INVALID_ARG;
   size_t ws = 0;
-  cpattn_status s = cpattn_prefill_workspace_size(q, k, q_base, n_chunks, mode, causal, &ws);
+  cpattn_status s = prefill_ws_bytes(q, k, q_base, n_chunks, mode, causal, nullptr, true, &ws);
   if (s != CPATTN_OK) return s;
   const size_t o_bytes = (size_t)q->b * q->s * q->h * q->d * elem_bytes(out_dtype);
   *bytes = align256(tensor_bytes(q)) + 2 * align256(tensor_bytes(k)) + align256(o_bytes) +

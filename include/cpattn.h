@@ -234,12 +234,15 @@ typedef enum { CPATTN_ASSIGN_CONTIGUOUS = 0, CPATTN_ASSIGN_ZIGZAG = 1 } cpattn_a
  *                        Pass-Q runs as SINGLE.  Tensor-core kernel only
  *                        (bf16, head_dim 128); otherwise PER_STEP.
  *   AUTO                 when the tensor-core kernel applies (bf16, head_dim
- *                        128) and the ring's work items are short -- fewer
- *                        than 48 visible 128-key tiles per 128-row query tile
- *                        on average, where a CTA's fixed start-up and
- *                        write-out cost is a large share of its work --
- *                        SINGLE_ONCHIP for Pass-KV and SINGLE for Pass-Q;
- *                        else PER_STEP.
+ *                        128): for Pass-KV, SINGLE_ONCHIP when the ring's
+ *                        work items are short -- fewer than 48 visible
+ *                        128-key tiles per 128-row query tile on average,
+ *                        where a CTA's fixed start-up and write-out cost is a
+ *                        large share of its work -- or when K and V take at
+ *                        most 96 MiB (they then stay in L2 while on-chip
+ *                        items stream different pieces), else PER_STEP; for
+ *                        Pass-Q, SINGLE when items are short, else PER_STEP.
+ *                        Without the tensor-core kernel: PER_STEP.
  * CPATTN_LAUNCH_DEFAULT (options NULL or launch = DEFAULT) is AUTO.
  */
 typedef enum {
@@ -345,6 +348,11 @@ cpattn_status cpattn_prefill_choose_mode_ex(const cpattn_tensor *q, const cpattn
  * device staging buffers the caller provides (`dev_scratch`, at least
  * cpattn_prefill_host_scratch_size bytes, 256-byte aligned), runs
  * cpattn_prefill there, copies O and LSE back, and synchronises `stream`.
+ * The copies overlap the ring: the first ring step starts on each Q piece as
+ * it lands and output pieces go back as soon as they are final.  Its launch
+ * mode is AUTO's with one difference: where work items are long it keeps one
+ * launch per ring step for Pass-KV (a single launch could not start before
+ * every input is in, nor return any output before the end).
  */
 cpattn_status cpattn_prefill_host_scratch_size(const cpattn_tensor *q, const cpattn_tensor *k,
                                                int64_t q_base, int n_chunks, int mode,

@@ -149,13 +149,16 @@ def test_workspace_sizes(lib):
 @pytest.mark.parametrize("shape,dtype,want_kv,want_q", [
     ((8192, 8192, 32, 8, 8), B.BF16, B.LAUNCH_SINGLE_ONCHIP, B.LAUNCH_SINGLE),   # 8-tile items
     ((2048, 32768, 16, 1, 8), B.BF16, B.LAUNCH_SINGLE_ONCHIP, B.LAUNCH_SINGLE),  # 32-tile items
-    ((131072, 131072, 16, 1, 16), B.BF16, B.LAUNCH_PER_STEP, B.LAUNCH_PER_STEP),  # ~60-tile
+    ((131072, 131072, 16, 1, 16), B.BF16, B.LAUNCH_SINGLE_ONCHIP, B.LAUNCH_PER_STEP),  # ~60-tile, K/V in L2
+    ((1048576, 1048576, 8, 1, 8), B.BF16, B.LAUNCH_PER_STEP, B.LAUNCH_PER_STEP),  # long items, K/V 512 MiB
     ((8192, 8192, 32, 8, 8), B.FP32, B.LAUNCH_PER_STEP, B.LAUNCH_PER_STEP),      # no tensor cores
 ])
 def test_auto_launch_mode(lib, shape, dtype, want_kv, want_q):
-    """CPATTN_LAUNCH_AUTO (the default) resolves to one launch for all ring
-    steps when work items are short (Pass-KV with its accumulator on chip),
-    one launch per step otherwise; the default workspace size is the
+    """CPATTN_LAUNCH_AUTO (the default) resolves, with the tensor-core kernel,
+    for Pass-KV to one launch with the accumulator on chip when work items
+    are short or K and V fit in L2, and for Pass-Q to one launch for all ring
+    steps when work items are short; otherwise, and without the tensor-core
+    kernel, to one launch per step.  The default workspace size is the
     resolved mode's."""
     sq, skv, hq, hkv, n = shape
     q_base = skv - sq

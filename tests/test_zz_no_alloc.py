@@ -53,8 +53,8 @@ def test_noalloc_matches_prefill_on_two_calls(B, mode):
 
 
 def test_noalloc_rejects_problems_beyond_its_buffer(B):
-    q, k, v = inputs(7, sq=65536, skv=65536, hq=4, hkv=1)   # Pass-KV needs 129 MiB
-    assert B.workspace_size(q, k, 8, 1) > (64 << 20)
+    q, k, v = inputs(7, sq=65536, skv=65536, hq=4, hkv=1)   # Pass-Q: fp32 partials, > 64 MiB
+    assert B.workspace_size(q, k, 8, 2) > (64 << 20)
     with pytest.raises(B.CpattnError) as err:
-        B.prefill_noalloc(q, k, v, 8, 1)
+        B.prefill_noalloc(q, k, v, 8, 2)
     assert err.value.status == 2   # CPATTN_ERR_UNSUPPORTED, nothing enqueued
