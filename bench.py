@@ -35,11 +35,17 @@ sys.path.insert(0, ROOT)
 METRIC = "CP prefill causal TFLOP/s & % of GB300 BF16 peak; ms/layer at 128K and 1M tokens"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
-# DRAM bytes (read + write) per tensor FLOP of the prefill attention kernel
-# from one ncu capture, and the kernel source it was taken from; the
-# roofline's traffic is null whenever the source differs from the capture.
-TRAFFIC_RECORD = {"sha": "4247d6041a1fae0a", "bytes_per_flop": 52.07e6 / 5.498e11,
-                  "capture": "profiles/attn_pair_32k_step.md"}
+# DRAM bytes (read + write) per tensor FLOP of each instance of the prefill
+# attention kernel (profiler kind) from one ncu capture, and the kernel source
+# it was taken from; the roofline's traffic is null whenever the source
+# differs from the capture or a timed launch has no record.
+TRAFFIC_RECORD = {
+    "attn_tc": {"sha": "4247d6041a1fae0a", "bytes_per_flop": 52.07e6 / 5.498e11,
+                "capture": "profiles/attn_pair_32k_step.md"},
+    "attn_tc_onchip": {"sha": "4247d6041a1fae0a", "bytes_per_flop": 244.05e6 / 4.398e12,
+                       "capture": "profiles/attn_pair_onchip_32k_passkv.md"},
+}
+ATTN_KINDS = ("attn_tc", "attn_tc_onchip")
 
 
 def load_peaks():
@@ -509,17 +515,19 @@ def main():
     value = world * flops_step * args.steps / (elapsed * 1e-3) / 1e12
 
     peaks, peak_src = load_peaks()
-    tc = [r for r in recs if r[0] == "attn_tc"]
+    tc = [r for r in recs if r[0] in ATTN_KINDS]
     tc_ms = sum(r[1] for r in tc)
     tc_flops = sum(r[2] for r in tc)
     achieved = tc_flops / (tc_ms * 1e-3) / 1e12 if tc_ms > 0 else None
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     traffic = None
-    if TRAFFIC_RECORD and TRAFFIC_RECORD.get("sha") == kernel_sha() and tc:
-        traffic = TRAFFIC_RECORD["bytes_per_flop"] * tc_flops / len(tc)
+    sha = kernel_sha()
+    if tc and all(TRAFFIC_RECORD.get(r[0], {}).get("sha") == sha for r in tc):
+        traffic = sum(TRAFFIC_RECORD[r[0]]["bytes_per_flop"] * r[2] for r in tc) / len(tc)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if achieved else None, "traffic": traffic,
-                "kernel": "attn_pair_kernel (tcgen05 cta_group::2 partial attention)",
+                "kernel": "attn_pair_kernel (tcgen05 cta_group::2 partial attention; "
+                          "per-step and on-chip instances)",
                 "peak_source": f"{peak_src} bf16 dense, sustained",
                 "launches_timed": len(tc), "avg_launch_ms": tc_ms / len(tc) if tc else None,
                 "share_of_step": tc_ms / elapsed if elapsed else None}

@@ -16,7 +16,7 @@ PASS_KV = 1
 PASS_Q = 2
 BF16, FP32 = 0, 1
 ROLE_NAMES = {0: "store", 1: "acc_init", 2: "acc_merge", 3: "acc_final", 4: "partial"}
-KERNEL_NAMES = {1: "attn_tc", 2: "attn_simt", 3: "merge2", 4: "mergeN", 5: "table"}
+KERNEL_NAMES = {1: "attn_tc", 2: "attn_simt", 3: "merge2", 4: "mergeN", 5: "table", 6: "attn_tc_onchip"}
 
 
 class CpattnTensor(ctypes.Structure):

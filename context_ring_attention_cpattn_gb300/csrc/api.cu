@@ -416,7 +416,10 @@ cudaError_t launch_attn(AttnParams &p, cudaStream_t st, const cpattn_tensor *q,
   const bool tc = attn_tc_supported(p);
   prof_before(st);
   cudaError_t e = tc ? launch_attn_tc(p, st) : launch_attn_simt(p, st);
-  prof_after(st, tc ? CPATTN_KERNEL_ATTN_TC : CPATTN_KERNEL_ATTN_SIMT, flops);
+  prof_after(st,
+             !tc ? CPATTN_KERNEL_ATTN_SIMT
+                 : (p.seg_groups ? CPATTN_KERNEL_ATTN_TC_ONCHIP : CPATTN_KERNEL_ATTN_TC),
+             flops);
   return e;
 }
 

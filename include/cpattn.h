@@ -422,7 +422,8 @@ typedef enum {
   CPATTN_KERNEL_ATTN_SIMT = 2,  /* fp32 / head_dim 64 partial-attention kernel */
   CPATTN_KERNEL_MERGE2 = 3,     /* pairwise LSE merge */
   CPATTN_KERNEL_MERGEN = 4,     /* N-way LSE merge of Pass-Q partials */
-  CPATTN_KERNEL_TABLE = 5       /* pair-table upload of a single-launch ring (work = bytes) */
+  CPATTN_KERNEL_TABLE = 5,      /* pair-table upload of a single-launch ring (work = bytes) */
+  CPATTN_KERNEL_ATTN_TC_ONCHIP = 6  /* tcgen05 kernel, Pass-KV with the accumulator on chip */
 } cpattn_kernel_kind;
 
 typedef struct {
