@@ -181,6 +181,34 @@ def test_auto_launch_mode(lib, shape, dtype, want_kv, want_q):
         assert a.value == b.value
 
 
+def test_host_call_keeps_per_step_for_long_items(lib):
+    """The host-buffer entry point overlaps its copies with the ring, so for
+    long items (the 128K shape) it keeps one launch per ring step: its scratch
+    is the staging buffers plus the per-step workspace (with the fp32
+    accumulator), while the device call at the same shape picks the on-chip
+    launch and needs only the pair table.  Short items (Llama-3-8B) take the
+    on-chip launch in both."""
+    align = lambda x: (x + 255) // 256 * 256
+    for (sq, hq, hkv, n), host_mode in (((131072, 16, 1, 16), B.LAUNCH_PER_STEP),
+                                        ((8192, 32, 8, 8), B.LAUNCH_SINGLE_ONCHIP)):
+        q, k = T(dtype=B.BF16, s=sq, h=hq), T(dtype=B.BF16, s=sq, h=hkv)
+        scratch, auto, explicit = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+        assert lib.cpattn_prefill_host_scratch_size(ctypes.byref(q), ctypes.byref(k), 0, n, 1, 1,
+                                                    B.BF16, ctypes.byref(scratch)) == 0
+        assert lib.cpattn_prefill_workspace_size(ctypes.byref(q), ctypes.byref(k), 0, n, 1, 1,
+                                                 ctypes.byref(auto)) == 0
+        assert lib.cpattn_prefill_workspace_size_ex(ctypes.byref(q), ctypes.byref(k), 0, n, 1, 1,
+                                                    ctypes.byref(B.PrefillOptions(0, host_mode)),
+                                                    ctypes.byref(explicit)) == 0
+        staging = (align(sq * hq * 128 * 2) + 2 * align(sq * hkv * 128 * 2) +
+                   align(sq * hq * 128 * 2) + align(hq * sq * 4))
+        assert scratch.value == staging + explicit.value
+        if host_mode == B.LAUNCH_PER_STEP:
+            assert explicit.value > auto.value + sq * hq * 128 * 4   # the accumulator
+        else:
+            assert explicit.value == auto.value
+
+
 def test_onchip_workspace_has_no_accumulator(lib):
     """SINGLE_ONCHIP Pass-KV keeps the accumulator on chip: its workspace is
     the pair table alone, SINGLE's adds progress counters and the fp32
