@@ -42,8 +42,8 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 TRAFFIC_RECORD = {
     "attn_tc": {"sha": "4247d6041a1fae0a", "bytes_per_flop": 52.07e6 / 5.498e11,
                 "capture": "profiles/attn_pair_32k_step.md"},
-    "attn_tc_onchip": {"sha": "4247d6041a1fae0a", "bytes_per_flop": 244.05e6 / 4.398e12,
-                       "capture": "profiles/attn_pair_onchip_32k_passkv.md"},
+    "attn_tc_onchip": {"sha": "4247d6041a1fae0a", "bytes_per_flop": 1.7117e9 / 7.0369e13,
+                       "capture": "profiles/attn_pair_onchip_128k_passkv.md"},
 }
 ATTN_KINDS = ("attn_tc", "attn_tc_onchip")
 
