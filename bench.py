@@ -531,6 +531,18 @@ def main():
                 "peak_source": f"{peak_src} bf16 dense, sustained",
                 "launches_timed": len(tc), "avg_launch_ms": tc_ms / len(tc) if tc else None,
                 "share_of_step": tc_ms / elapsed if elapsed else None}
+    # The same figures per kernel instance (the step mixes Pass-KV's on-chip
+    # launch with Pass-Q's per-step launches at 128K).
+    by_inst = {}
+    for kind in ATTN_KINDS:
+        rk = [r for r in tc if r[0] == kind]
+        ms_k = sum(r[1] for r in rk)
+        if rk and ms_k > 0:
+            ach = sum(r[2] for r in rk) / (ms_k * 1e-3) / 1e12
+            by_inst[kind] = {"launches": len(rk), "achieved": ach, "frac": ach / peak,
+                             "share_of_step": ms_k / elapsed if elapsed else None,
+                             "capture": TRAFFIC_RECORD.get(kind, {}).get("capture")}
+    roofline["by_instance"] = by_inst
 
     ms_layer = {names[m]: statistics.median(per_mode[m]) for m in modes}
     # Load balance of the ring this single GPU emulates: on N GPUs each ring
