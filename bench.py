@@ -638,13 +638,20 @@ def main():
         torch.cuda.empty_cache()
         scratch = torch.empty(need, dtype=torch.uint8, device="cuda")
 
+        per_call = {names[m]: [] for m in modes}
+
         def host_step():
+            # Each call returns with its stream synchronised: wall time per call.
             for m in modes:
+                t = time.perf_counter()
                 B.prefill_host(qh, kh, vh, w.n_chunks, m, oh, lh, scratch, q_base=w.q_base,
                                causal=w.causal)
+                per_call[names[m]].append(1e3 * (time.perf_counter() - t))
 
         for _ in range(args.warmup):
             host_step()
+        for m in modes:
+            per_call[names[m]].clear()
         barrier(world)
         t0 = time.perf_counter()
         for _ in range(args.steps):
@@ -656,6 +663,7 @@ def main():
                "h2d_bytes_per_step": len(modes) * in_bytes,
                "d2h_bytes_per_step": len(modes) * out_bytes,
                "ms_per_step": 1e3 * t_e2e / args.steps,
+               "ms_per_call": {k: statistics.median(x) for k, x in per_call.items() if x},
                "path": "cpattn_prefill_host (pinned host buffers; copies inside the timed region)"}
         del scratch
 

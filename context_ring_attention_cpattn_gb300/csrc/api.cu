@@ -447,13 +447,9 @@ constexpr double kAutoSingleTiles = 48.0;
 // (the GPU has 126 MB).
 constexpr double kOnchipKvBytes = 96.0 * 1024 * 1024;
 
-// pipelined_io: the call overlaps host copies with the ring (the host-buffer
-// entry point), which one launch for all steps cannot do; it then keeps one
-// launch per step wherever items are long.
-int resolve_launch(int lmode, const Plan &pl, const cpattn_tensor *q, const cpattn_tensor *k,
-                   int64_t q_base, int causal, bool pipelined_io = false) {
-  if (lmode != CPATTN_LAUNCH_AUTO) return lmode;
-  if (q->dtype != CPATTN_BF16 || q->d != 128) return CPATTN_LAUNCH_PER_STEP;  // no tensor-core kernel
+// Work items are short when a 128-row query tile sees, on average over the
+// ring's pairs, fewer than kAutoSingleTiles visible 128-key tiles.
+bool short_items(const Plan &pl, int64_t q_base, int causal) {
   double vis = 0.0, rows = 0.0;
   for (const auto &e : pl.entries) {
     const int64_t delta = q_base + (int64_t)e.q_chunk * pl.Cq - (int64_t)e.kv_chunk * pl.C;
@@ -461,7 +457,14 @@ int resolve_launch(int lmode, const Plan &pl, const cpattn_tensor *q, const cpat
     rows += (double)pl.Cq;
   }
   const double tiles = rows > 0.0 ? vis / rows / 128.0 : 0.0;
-  const bool short_items = tiles < kAutoSingleTiles;
+  return tiles < kAutoSingleTiles;
+}
+
+int resolve_launch(int lmode, const Plan &pl, const cpattn_tensor *q, const cpattn_tensor *k,
+                   int64_t q_base, int causal) {
+  if (lmode != CPATTN_LAUNCH_AUTO) return lmode;
+  if (q->dtype != CPATTN_BF16 || q->d != 128) return CPATTN_LAUNCH_PER_STEP;  // no tensor-core kernel
+  const bool short_it = short_items(pl, q_base, causal);
   if (pl.mode == CPATTN_PASS_KV) {
     // The accumulator on chip (no fp32 round trip per visit) when items are
     // short or K and V stay in L2: an on-chip item streams its own sequence
@@ -469,11 +472,40 @@ int resolve_launch(int lmode, const Plan &pl, const cpattn_tensor *q, const cpat
     // hold only for a small K/V.  Measured on one GB300: 128K (K/V 64 MiB)
     // 44.5 vs 49.6 ms per layer per step; 1M (K/V 512 MiB) 1718 vs 1362 ms.
     const double kv_bytes = (double)k->b * (double)k->s * (double)k->h * (double)k->d * 2.0 * 2.0;
-    return (short_items || (!pipelined_io && kv_bytes <= kOnchipKvBytes))
-               ? CPATTN_LAUNCH_SINGLE_ONCHIP
-               : CPATTN_LAUNCH_PER_STEP;
+    return (short_it || kv_bytes <= kOnchipKvBytes) ? CPATTN_LAUNCH_SINGLE_ONCHIP
+                                                     : CPATTN_LAUNCH_PER_STEP;
   }
-  return short_items ? CPATTN_LAUNCH_SINGLE : CPATTN_LAUNCH_PER_STEP;
+  return short_it ? CPATTN_LAUNCH_SINGLE : CPATTN_LAUNCH_PER_STEP;
+}
+
+// Launch groups of an on-chip Pass-KV ring: one group of all Q pieces, or,
+// when a host-buffer call streams Q in piece by piece (long items only),
+// consecutive groups in arrival order: a small first group, so the first
+// launch starts once K/V and a few pieces are in, then three of about equal
+// size, so a group's output goes back while the later groups run and only
+// the last group's copy is left at the end.  Each piece's work items are the
+// same in every grouping (bitwise-equal results).
+std::vector<std::vector<int>> onchip_groups(int P, bool split) {
+  std::vector<std::vector<int>> groups;
+  auto add = [&](int a, int b) {
+    groups.emplace_back();
+    for (int i = a; i < b; ++i) groups.back().push_back(i);
+  };
+  if (!split || P < 4) {
+    add(0, P);
+    return groups;
+  }
+  const int n = P >= 8 ? 4 : 2;
+  const int first = std::max(1, P / 8);
+  add(0, first);
+  const int rest = P - first, m = n - 1;
+  int at = first;
+  for (int x = 0; x < m; ++x) {
+    const int size = rest / m + (x < rest % m ? 1 : 0);
+    add(at, at + size);
+    at += size;
+  }
+  return groups;
 }
 
 // Called (at enqueue time, on the host) once the work that finalises output
@@ -497,7 +529,7 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
     return s;
   int lmode = launch_mode_of(opts);
   if (!valid_launch(lmode)) return CPATTN_ERR_INVALID_ARG;
-  lmode = resolve_launch(lmode, pl, q, k, q_base, causal, on_final != nullptr || on_inputs != nullptr);
+  lmode = resolve_launch(lmode, pl, q, k, q_base, causal);
   const bool onchip = lmode == CPATTN_LAUNCH_SINGLE_ONCHIP && pl.mode == CPATTN_PASS_KV;
   const bool single = lmode == CPATTN_LAUNCH_SINGLE || lmode == CPATTN_LAUNCH_SINGLE_ONCHIP;
   const WsLayout wl = ws_layout(pl, q->b, q->s, q->h, q->d, lmode);
@@ -537,11 +569,11 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
     p.part_lse_stride = wl.slot_lse_elems;
   }
 
-  // Pairs of each launch ordered by work, largest first.
-  auto launch_items = [&](size_t e0, size_t e1, std::vector<PairDesc> &out) {
+  // Pairs of the plan entries `idx` ordered by work, largest first.
+  auto launch_items_of = [&](const std::vector<size_t> &idx, std::vector<PairDesc> &out) {
     struct Item { PairDesc pd; double work; };
     std::vector<Item> items;
-    for (size_t x = e0; x < e1; ++x) {
+    for (size_t x : idx) {
       const cpattn_plan_entry &e = pl.entries[x];
       Item it;
       memset(&it.pd, 0, sizeof(it.pd));
@@ -560,9 +592,18 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
                      [](const Item &a, const Item &b) { return a.work > b.work; });
     for (const auto &it : items) out.push_back(it.pd);
   };
+  // ... of one launch of the plan: entries [e0, e1).
+  auto launch_items = [&](size_t e0, size_t e1, std::vector<PairDesc> &out) {
+    std::vector<size_t> idx;
+    for (size_t x = e0; x < e1; ++x) idx.push_back(x);
+    launch_items_of(idx, out);
+  };
 
+  // Host-buffer calls with long items split the on-chip launch into groups
+  // of Q pieces (onchip_groups); every group's rows go back after its launch.
+  const bool grouped = onchip && on_inputs != nullptr && !short_items(pl, q_base, causal);
   if (single && attn_tc_supported(p)) {
-    NvtxRange range("cpattn %s ring, one launch", mode_name(mode));
+    NvtxRange range("cpattn %s ring, one launch%s", mode_name(mode), grouped ? " per group" : "");
     std::vector<PairDesc> table;
     size_t e0 = 0;
     for (int l = 0; l < pl.n_launches; ++l) {
@@ -573,62 +614,15 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
     }
     const TcItemShape sh = attn_tc_item_shape(p);
     const int per_tile = (int)(q->h / sh.heads) * (int)q->b;
-    int total = 0;
-    double vis = 0.0;
-    for (const auto &pd : table) vis += visible_pairs(pd.delta, pd.q_len, 0, pd.kv_len, causal != 0);
-    if (onchip) {
-      // Each Q piece's pairs in ring order form one run of work items: a
-      // work item streams every visiting K/V piece through one on-chip
-      // accumulator and stores the result (segment x: visit = x, slot = the
-      // run's length).  Runs with the most work first.
-      std::vector<std::vector<PairDesc>> runs(pl.P);
-      std::vector<double> work(pl.P, 0.0);
-      for (const auto &pd : table) {
-        const int piece = (int)(pd.q_row0 / pl.Cq);
-        runs[piece].push_back(pd);
-        work[piece] += visible_pairs(pd.delta, pd.q_len, 0, pd.kv_len, causal != 0);
-      }
-      std::vector<int> order;
-      for (int i = 0; i < pl.P; ++i)
-        if (!runs[i].empty()) order.push_back(i);
-      std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return work[a] > work[b]; });
-      table.clear();
-      for (int i : order) {
-        const int n = (int)runs[i].size();
-        const int n_qtiles = (runs[i][0].q_len + sh.rows - 1) / sh.rows;
-        for (int x = 0; x < n; ++x) {
-          PairDesc pd = runs[i][x];
-          pd.mode = kStore;
-          pd.visit = x;
-          pd.slot = n;
-          pd.n_qtiles = n_qtiles;
-          pd.cta_begin = total;
-          table.push_back(pd);
-        }
-        total += n_qtiles * per_tile;
-      }
-    } else {
-      // Work items keep the ring's launch order; a Pass-KV accumulator
-      // update waits (bounded) until the previous visit of the same rows has
-      // finished.
-      std::vector<int> visits(pl.P, 0);
-      for (auto &pd : table) {
-        pd.n_qtiles = (pd.q_len + sh.rows - 1) / sh.rows;
-        pd.cta_begin = total;
-        total += pd.n_qtiles * per_tile;
-        const int piece = (int)(pd.q_row0 / pl.Cq);
-        if (pd.mode == kAccInit || pd.mode == kAccMerge || pd.mode == kAccFinal)
-          pd.visit = visits[piece]++;
-      }
-    }
-    // Inputs arriving piece by piece: the one launch reads all of them.
-    for (int i = 0; i < pl.P && on_inputs != nullptr; ++i)
-      if ((*on_inputs)(i, 0) != cudaSuccess) return CPATTN_ERR_CUDA;
-    if (total > 0) {
-      PairDesc *dev_table = reinterpret_cast<PairDesc *>(ws + wl.table);
-      if (upload_table(dev_table, table, st) != cudaSuccess) return CPATTN_ERR_CUDA;
-      p.pair_table = dev_table;
-      p.n_table = (int32_t)table.size();
+    PairDesc *dev_table = reinterpret_cast<PairDesc *>(ws + wl.table);
+    // One launch over `lt` (total work items, visible pairs) after its
+    // inputs are in; the table goes to dev_table + t_off.
+    size_t t_off = 0;
+    auto launch_table = [&](const std::vector<PairDesc> &lt, int total, double vis) -> cpattn_status {
+      if (total == 0) return CPATTN_OK;
+      if (upload_table(dev_table + t_off, lt, st) != cudaSuccess) return CPATTN_ERR_CUDA;
+      p.pair_table = dev_table + t_off;
+      p.n_table = (int32_t)lt.size();
       p.total_ctas = total;
       p.persistent_ctas = 1;
       p.seg_groups = onchip ? 1 : 0;
@@ -639,12 +633,78 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
           return CPATTN_ERR_CUDA;
       }
       if (launch_attn(p, st, q, vis) != cudaSuccess) return CPATTN_ERR_CUDA;
+      t_off += lt.size();
       p.pair_table = nullptr;
       p.n_table = 0;
       p.dep_counters = nullptr;
       p.dep_hold = 0;
       p.persistent_ctas = 0;
       p.seg_groups = 0;
+      return CPATTN_OK;
+    };
+    if (onchip) {
+      // Each Q piece's pairs in ring order form one run of work items: a
+      // work item streams every visiting K/V piece through one on-chip
+      // accumulator and stores the result (segment x: visit = x, slot = the
+      // run's length).  Within a launch, runs with the most work first.
+      std::vector<std::vector<PairDesc>> runs(pl.P);
+      std::vector<double> work(pl.P, 0.0);
+      for (const auto &pd : table) {
+        const int piece = (int)(pd.q_row0 / pl.Cq);
+        runs[piece].push_back(pd);
+        work[piece] += visible_pairs(pd.delta, pd.q_len, 0, pd.kv_len, causal != 0);
+      }
+      for (const auto &grp : onchip_groups(pl.P, grouped)) {
+        std::vector<int> order;
+        for (int i : grp)
+          if (!runs[i].empty()) order.push_back(i);
+        std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return work[a] > work[b]; });
+        std::vector<PairDesc> lt;
+        int total = 0;
+        double vis = 0.0;
+        for (int i : order) {
+          const int n = (int)runs[i].size();
+          const int n_qtiles = (runs[i][0].q_len + sh.rows - 1) / sh.rows;
+          for (int x = 0; x < n; ++x) {
+            PairDesc pd = runs[i][x];
+            pd.mode = kStore;
+            pd.visit = x;
+            pd.slot = n;
+            pd.n_qtiles = n_qtiles;
+            pd.cta_begin = total;
+            lt.push_back(pd);
+          }
+          total += n_qtiles * per_tile;
+          vis += work[i];
+        }
+        // Inputs arriving piece by piece: the launch reads all of its pieces.
+        for (int i : grp)
+          if (on_inputs != nullptr && (*on_inputs)(i, 0) != cudaSuccess) return CPATTN_ERR_CUDA;
+        if ((s = launch_table(lt, total, vis)) != CPATTN_OK) return s;
+        for (int i : order)
+          if (grouped && on_final != nullptr && (*on_final)(i * pl.Cq, pl.Cq) != cudaSuccess)
+            return CPATTN_ERR_CUDA;
+      }
+    } else {
+      // Work items keep the ring's launch order; a Pass-KV accumulator
+      // update waits (bounded) until the previous visit of the same rows has
+      // finished.
+      int total = 0;
+      double vis = 0.0;
+      std::vector<int> visits(pl.P, 0);
+      for (auto &pd : table) {
+        pd.n_qtiles = (pd.q_len + sh.rows - 1) / sh.rows;
+        pd.cta_begin = total;
+        total += pd.n_qtiles * per_tile;
+        vis += visible_pairs(pd.delta, pd.q_len, 0, pd.kv_len, causal != 0);
+        const int piece = (int)(pd.q_row0 / pl.Cq);
+        if (pd.mode == kAccInit || pd.mode == kAccMerge || pd.mode == kAccFinal)
+          pd.visit = visits[piece]++;
+      }
+      // Inputs arriving piece by piece: the one launch reads all of them.
+      for (int i = 0; i < pl.P && on_inputs != nullptr; ++i)
+        if ((*on_inputs)(i, 0) != cudaSuccess) return CPATTN_ERR_CUDA;
+      if ((s = launch_table(table, total, vis)) != CPATTN_OK) return s;
     }
   }
   const bool per_step = !(single && attn_tc_supported(p));
@@ -698,11 +758,51 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
     if (e.role == CPATTN_ROLE_PARTIAL) last_launch[e.q_chunk] = std::max(last_launch[e.q_chunk], e.launch);
   std::vector<bool> merged(pl.P, false);
 
+  p.persistent_ctas = lmode == CPATTN_LAUNCH_PERSISTENT_STEP ? 1 : 0;
+  // Host-buffer Pass-Q calls with long items: every Q piece completes only at
+  // the ring's last step, so merges and output copies would all wait for the
+  // end.  They run the ring's pairs grouped by Q piece instead (the groups of
+  // onchip_groups, in arrival order): each pair is computed exactly as in its
+  // ring step and each piece is merged in the same order, so the result is
+  // the same bit for bit, but a group's merge and output copy overlap the
+  // later groups.
+  const bool q_grouped = per_step && pl.mode == CPATTN_PASS_Q && on_inputs != nullptr &&
+                         on_final != nullptr && !short_items(pl, q_base, causal);
+  if (q_grouped) {
+    for (const auto &grp : onchip_groups(pl.P, true)) {
+      NvtxRange range("cpattn %s pieces %d..%d", mode_name(mode), grp.front(), grp.back());
+      std::vector<bool> in(pl.P, false);
+      for (int i : grp) in[i] = true;
+      std::vector<size_t> idx;
+      for (size_t x = 0; x < pl.entries.size(); ++x)
+        if (in[pl.entries[x].q_chunk]) idx.push_back(x);
+      std::vector<PairDesc> items;
+      launch_items_of(idx, items);
+      for (int i : grp)
+        if ((*on_inputs)(i, 0) != cudaSuccess) return CPATTN_ERR_CUDA;
+      for (size_t x0 = 0; x0 < items.size(); x0 += kMaxPairs) {
+        const size_t n = std::min<size_t>(kMaxPairs, items.size() - x0);
+        p.n_pairs = (int32_t)n;
+        for (size_t x = 0; x < n; ++x) p.pairs[x] = items[x0 + x];
+        if (launch_attn(p, st, q) != cudaSuccess) return CPATTN_ERR_CUDA;
+      }
+      std::vector<int> ready;
+      for (int i : grp) {
+        if (needs_merge_launch(i)) {
+          ready.push_back(i);
+          merged[i] = true;
+        } else if ((*on_final)(i * pl.Cq, pl.Cq) != cudaSuccess) {  // one pair: stored directly
+          return CPATTN_ERR_CUDA;
+        }
+      }
+      if ((s = merge_pieces(ready)) != CPATTN_OK) return s;
+    }
+  }
+
   // One launch per ring step (two per step for zigzag Pass-KV, one per
   // visiting K/V piece).
-  p.persistent_ctas = lmode == CPATTN_LAUNCH_PERSISTENT_STEP ? 1 : 0;
   size_t e0 = 0;
-  for (int l = 0; l < pl.n_launches && per_step; ++l) {
+  for (int l = 0; l < pl.n_launches && per_step && !q_grouped; ++l) {
     size_t e1 = e0;
     while (e1 < pl.entries.size() && pl.entries[e1].launch == l) ++e1;
     if (e1 == e0) continue;
@@ -750,8 +850,15 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
   for (int i = 0; i < pl.P; ++i)
     if (needs_merge_launch(i) && !merged[i]) rest.push_back(i);
   if ((s = merge_pieces(rest)) != CPATTN_OK) return s;
-  if (!per_step && on_final != nullptr && (*on_final)(0, q->s) != cudaSuccess)
-    return CPATTN_ERR_CUDA;
+  if (!per_step && on_final != nullptr) {
+    if (grouped) {
+      // Rows of pieces no key reaches (written by the merge launch above).
+      for (int i : rest)
+        if ((*on_final)(i * pl.Cq, pl.Cq) != cudaSuccess) return CPATTN_ERR_CUDA;
+    } else if ((*on_final)(0, q->s) != cudaSuccess) {
+      return CPATTN_ERR_CUDA;
+    }
+  }
   return CPATTN_OK;
 }
 
@@ -922,8 +1029,7 @@ cpattn_status cpattn_prefill_workspace_size(const cpattn_tensor *q, const cpattn
 
 static cpattn_status prefill_ws_bytes(const cpattn_tensor *q, const cpattn_tensor *k, int64_t q_base,
                                int n_chunks, int mode, int causal,
-                               const cpattn_prefill_options *opts, bool pipelined_io,
-                               size_t *bytes) {
+                               const cpattn_prefill_options *opts, size_t *bytes) {
   try {
     if (bytes == nullptr) return CPATTN_ERR_INVALID_ARG;
     cpattn_status s = check_view(q);
@@ -934,7 +1040,7 @@ static cpattn_status prefill_ws_bytes(const cpattn_tensor *q, const cpattn_tenso
         CPATTN_OK)
       return s;
     if (!valid_launch(launch_mode_of(opts))) return CPATTN_ERR_INVALID_ARG;
-    const int lmode = resolve_launch(launch_mode_of(opts), pl, q, k, q_base, causal, pipelined_io);
+    const int lmode = resolve_launch(launch_mode_of(opts), pl, q, k, q_base, causal);
     *bytes = ws_layout(pl, q->b, q->s, q->h, q->d, lmode).total;
     return CPATTN_OK;
   } catch (...) {
@@ -945,7 +1051,7 @@ static cpattn_status prefill_ws_bytes(const cpattn_tensor *q, const cpattn_tenso
 cpattn_status cpattn_prefill_workspace_size_ex(const cpattn_tensor *q, const cpattn_tensor *k,
                                                int64_t q_base, int n_chunks, int mode, int causal,
                                                const cpattn_prefill_options *opts, size_t *bytes) {
-  return prefill_ws_bytes(q, k, q_base, n_chunks, mode, causal, opts, false, bytes);
+  return prefill_ws_bytes(q, k, q_base, n_chunks, mode, causal, opts, bytes);
 }
 
 cpattn_status cpattn_prefill_launch_mode(const cpattn_tensor *q, const cpattn_tensor *k,
@@ -1210,7 +1316,7 @@ cpattn_status cpattn_prefill_host_scratch_size(const cpattn_tensor *q, const cpa
                                                int out_dtype, size_t *bytes) {
   if (bytes == nullptr || elem_bytes(out_dtype) == 0) return CPATTN_ERR_INVALID_ARG;
   size_t ws = 0;
-  cpattn_status s = prefill_ws_bytes(q, k, q_base, n_chunks, mode, causal, nullptr, true, &ws);
+  cpattn_status s = prefill_ws_bytes(q, k, q_base, n_chunks, mode, causal, nullptr, &ws);
   if (s != CPATTN_OK) return s;
   const size_t o_bytes = (size_t)q->b * q->s * q->h * q->d * elem_bytes(out_dtype);
   *bytes = align256(tensor_bytes(q)) + 2 * align256(tensor_bytes(k)) + align256(o_bytes) +

@@ -348,11 +348,15 @@ cpattn_status cpattn_prefill_choose_mode_ex(const cpattn_tensor *q, const cpattn
  * device staging buffers the caller provides (`dev_scratch`, at least
  * cpattn_prefill_host_scratch_size bytes, 256-byte aligned), runs
  * cpattn_prefill there, copies O and LSE back, and synchronises `stream`.
- * The copies overlap the ring: the first ring step starts on each Q piece as
- * it lands and output pieces go back as soon as they are final.  Its launch
- * mode is AUTO's with one difference: where work items are long it keeps one
- * launch per ring step for Pass-KV (a single launch could not start before
- * every input is in, nor return any output before the end).
+ * The copies overlap the ring: Q goes up one piece at a time after K and V,
+ * work starts on each piece once it has landed, and output pieces go back as
+ * soon as they are final.  The launch mode is AUTO's.  One launch per ring
+ * step: the first step runs one launch per pair, each as its Q piece lands.
+ * The on-chip Pass-KV launch with long work items: split into up to four
+ * launches over consecutive groups of Q pieces (a small first group, then
+ * three of about equal size), each started once its pieces are in and each
+ * group's rows copied back while the later groups run.  A piece's work items
+ * are the same in every split, so results equal cpattn_prefill's bit for bit.
  */
 cpattn_status cpattn_prefill_host_scratch_size(const cpattn_tensor *q, const cpattn_tensor *k,
                                                int64_t q_base, int n_chunks, int mode,

@@ -181,32 +181,27 @@ def test_auto_launch_mode(lib, shape, dtype, want_kv, want_q):
         assert a.value == b.value
 
 
-def test_host_call_keeps_per_step_for_long_items(lib):
-    """The host-buffer entry point overlaps its copies with the ring, so for
-    long items (the 128K shape) it keeps one launch per ring step: its scratch
-    is the staging buffers plus the per-step workspace (with the fp32
-    accumulator), while the device call at the same shape picks the on-chip
-    launch and needs only the pair table.  Short items (Llama-3-8B) take the
-    on-chip launch in both."""
+def test_host_call_takes_the_device_launch_mode(lib):
+    """The host-buffer entry point runs the launch mode AUTO picks for the
+    device call (at the 128K shape it splits the on-chip Pass-KV launch into
+    groups of Q pieces, which needs no more workspace): its scratch is the
+    staging buffers plus the device call's workspace, the pair table only, with
+    no fp32 accumulator, for long (128K) and short (Llama-3-8B) items alike."""
     align = lambda x: (x + 255) // 256 * 256
-    for (sq, hq, hkv, n), host_mode in (((131072, 16, 1, 16), B.LAUNCH_PER_STEP),
-                                        ((8192, 32, 8, 8), B.LAUNCH_SINGLE_ONCHIP)):
+    for sq, hq, hkv, n in ((131072, 16, 1, 16), (8192, 32, 8, 8)):
         q, k = T(dtype=B.BF16, s=sq, h=hq), T(dtype=B.BF16, s=sq, h=hkv)
-        scratch, auto, explicit = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+        scratch, auto, launch = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_int()
         assert lib.cpattn_prefill_host_scratch_size(ctypes.byref(q), ctypes.byref(k), 0, n, 1, 1,
                                                     B.BF16, ctypes.byref(scratch)) == 0
         assert lib.cpattn_prefill_workspace_size(ctypes.byref(q), ctypes.byref(k), 0, n, 1, 1,
                                                  ctypes.byref(auto)) == 0
-        assert lib.cpattn_prefill_workspace_size_ex(ctypes.byref(q), ctypes.byref(k), 0, n, 1, 1,
-                                                    ctypes.byref(B.PrefillOptions(0, host_mode)),
-                                                    ctypes.byref(explicit)) == 0
+        assert lib.cpattn_prefill_launch_mode(ctypes.byref(q), ctypes.byref(k), 0, n, 1, 1, None,
+                                              ctypes.byref(launch)) == 0
+        assert launch.value == B.LAUNCH_SINGLE_ONCHIP
         staging = (align(sq * hq * 128 * 2) + 2 * align(sq * hkv * 128 * 2) +
                    align(sq * hq * 128 * 2) + align(hq * sq * 4))
-        assert scratch.value == staging + explicit.value
-        if host_mode == B.LAUNCH_PER_STEP:
-            assert explicit.value > auto.value + sq * hq * 128 * 4   # the accumulator
-        else:
-            assert explicit.value == auto.value
+        assert scratch.value == staging + auto.value
+        assert auto.value < sq * hq * 128 * 4   # no accumulator
 
 
 def test_onchip_workspace_has_no_accumulator(lib):

@@ -102,6 +102,45 @@ def test_prefill_host_entry_point(B, mode, name, batch):
     assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())
 
 
+@pytest.mark.parametrize("mode", [1, 2])
+def test_prefill_host_groups_long_items(B, mode):
+    """Long items (65536 causal tokens, 8 chunks of 8192, 16/1 heads): the
+    host-buffer call works through consecutive groups of Q pieces ({0},
+    {1..3}, {4, 5}, {6, 7}) so that copies overlap the work -- Pass-KV as four
+    on-chip launches, Pass-Q as the ring's pairs grouped by Q piece with each
+    group's merge before the next group's pairs -- and gives the device
+    call's result bit for bit."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(65536)
+    sq, n = 65536, 8
+    q = torch.randn((1, sq, 16, 128), generator=g, device="cuda").to(torch.bfloat16)
+    k = torch.randn((1, sq, 1, 128), generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn((1, sq, 1, 128), generator=g, device="cuda").to(torch.bfloat16)
+    o_ref, l_ref = B.prefill(q, k, v, n, mode)
+    o_ref, l_ref = o_ref.cpu(), l_ref.cpu()
+    torch.cuda.empty_cache()
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = torch.full_like(qh, float("nan")).pin_memory()
+    lh = torch.full((1, 16, sq), float("nan"), dtype=torch.float32).pin_memory()
+    scratch = torch.empty(B.host_scratch_size(qh, kh, n, mode), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    B.profile_begin(256)
+    try:
+        B.prefill_host(qh, kh, vh, n, mode, oh, lh, scratch)
+    finally:
+        recs = B.profile_end(256)
+    kinds = [r[0] for r in recs if r[0] != "table"]
+    if mode == B.PASS_KV:
+        assert B.launch_mode(q, k, n, mode) == B.LAUNCH_SINGLE_ONCHIP
+        assert kinds == ["attn_tc_onchip"] * 4
+    else:
+        assert B.launch_mode(q, k, n, mode) == B.LAUNCH_PER_STEP
+        # four groups, each: its pairs, then the merge of its pieces (piece 0
+        # has one pair, stored directly)
+        assert kinds == ["attn_tc"] + ["attn_tc", "mergeN"] * 3
+    assert torch.equal(oh, o_ref) and torch.equal(lh, l_ref)
+
+
 @pytest.mark.parametrize("name", ["tiny", "llama3-8b", "partial-32k", "128k"])
 def test_prefill_zigzag_assignment(B, name):
     """Zigzag chunk-to-rank assignment (rank r holds pieces r and 2N-1-r) gives
