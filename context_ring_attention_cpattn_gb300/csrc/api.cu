@@ -478,14 +478,15 @@ int resolve_launch(int lmode, const Plan &pl, const cpattn_tensor *q, const cpat
   return short_it ? CPATTN_LAUNCH_SINGLE : CPATTN_LAUNCH_PER_STEP;
 }
 
-// Launch groups of an on-chip Pass-KV ring: one group of all Q pieces, or,
-// when a host-buffer call streams Q in piece by piece (long items only),
-// consecutive groups in arrival order: a small first group, so the first
-// launch starts once K/V and a few pieces are in, then three of about equal
-// size, so a group's output goes back while the later groups run and only
-// the last group's copy is left at the end.  Each piece's work items are the
-// same in every grouping (bitwise-equal results).
-std::vector<std::vector<int>> onchip_groups(int P, bool split) {
+// Groups of Q pieces for a host-buffer call that streams Q in piece by piece
+// and copies output back as it becomes final (long items only; otherwise one
+// group of all pieces).  In arrival order: a small first group, so work starts
+// once K/V and a few pieces are in; up to three middle groups of about equal
+// size, each started once its pieces are in, whose output goes back while the
+// later groups run; and the last piece alone, so that only its own output
+// (and, for Pass-Q, its merge) is left when the work ends.  A piece's work
+// items are the same in every grouping (bitwise-equal results).
+std::vector<std::vector<int>> piece_groups(int P, bool split) {
   std::vector<std::vector<int>> groups;
   auto add = [&](int a, int b) {
     groups.emplace_back();
@@ -495,16 +496,16 @@ std::vector<std::vector<int>> onchip_groups(int P, bool split) {
     add(0, P);
     return groups;
   }
-  const int n = P >= 8 ? 4 : 2;
   const int first = std::max(1, P / 8);
   add(0, first);
-  const int rest = P - first, m = n - 1;
+  const int middle = P - first - 1, m = std::min(3, middle);
   int at = first;
   for (int x = 0; x < m; ++x) {
-    const int size = rest / m + (x < rest % m ? 1 : 0);
+    const int size = middle / m + (x >= m - middle % m ? 1 : 0);
     add(at, at + size);
     at += size;
   }
+  add(P - 1, P);
   return groups;
 }
 
@@ -600,7 +601,7 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
   };
 
   // Host-buffer calls with long items split the on-chip launch into groups
-  // of Q pieces (onchip_groups); every group's rows go back after its launch.
+  // of Q pieces (piece_groups); every group's rows go back after its launch.
   const bool grouped = onchip && on_inputs != nullptr && !short_items(pl, q_base, causal);
   if (single && attn_tc_supported(p)) {
     NvtxRange range("cpattn %s ring, one launch%s", mode_name(mode), grouped ? " per group" : "");
@@ -654,7 +655,7 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
         runs[piece].push_back(pd);
         work[piece] += visible_pairs(pd.delta, pd.q_len, 0, pd.kv_len, causal != 0);
       }
-      for (const auto &grp : onchip_groups(pl.P, grouped)) {
+      for (const auto &grp : piece_groups(pl.P, grouped)) {
         std::vector<int> order;
         for (int i : grp)
           if (!runs[i].empty()) order.push_back(i);
@@ -762,14 +763,14 @@ cpattn_status prefill_impl(const cpattn_tensor *q, const cpattn_tensor *k, const
   // Host-buffer Pass-Q calls with long items: every Q piece completes only at
   // the ring's last step, so merges and output copies would all wait for the
   // end.  They run the ring's pairs grouped by Q piece instead (the groups of
-  // onchip_groups, in arrival order): each pair is computed exactly as in its
+  // piece_groups, in arrival order): each pair is computed exactly as in its
   // ring step and each piece is merged in the same order, so the result is
   // the same bit for bit, but a group's merge and output copy overlap the
   // later groups.
   const bool q_grouped = per_step && pl.mode == CPATTN_PASS_Q && on_inputs != nullptr &&
                          on_final != nullptr && !short_items(pl, q_base, causal);
   if (q_grouped) {
-    for (const auto &grp : onchip_groups(pl.P, true)) {
+    for (const auto &grp : piece_groups(pl.P, true)) {
       NvtxRange range("cpattn %s pieces %d..%d", mode_name(mode), grp.front(), grp.back());
       std::vector<bool> in(pl.P, false);
       for (int i : grp) in[i] = true;

@@ -352,11 +352,14 @@ cpattn_status cpattn_prefill_choose_mode_ex(const cpattn_tensor *q, const cpattn
  * work starts on each piece once it has landed, and output pieces go back as
  * soon as they are final.  The launch mode is AUTO's.  One launch per ring
  * step: the first step runs one launch per pair, each as its Q piece lands.
- * The on-chip Pass-KV launch with long work items: split into up to four
- * launches over consecutive groups of Q pieces (a small first group, then
- * three of about equal size), each started once its pieces are in and each
- * group's rows copied back while the later groups run.  A piece's work items
- * are the same in every split, so results equal cpattn_prefill's bit for bit.
+ * Where work items are long the call works through consecutive groups of Q
+ * pieces in arrival order (a small first group, up to three of about equal
+ * size, then the last piece alone), each started once its pieces are in and
+ * each group's rows copied back while the later groups run: the on-chip
+ * Pass-KV launch becomes one launch per group, and Pass-Q runs the ring's
+ * pairs grouped by Q piece, each group merged right after its pairs.  Every
+ * pair and merge is computed as in cpattn_prefill, so results equal its bit
+ * for bit.
  */
 cpattn_status cpattn_prefill_host_scratch_size(const cpattn_tensor *q, const cpattn_tensor *k,
                                                int64_t q_base, int n_chunks, int mode,

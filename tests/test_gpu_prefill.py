@@ -106,9 +106,9 @@ def test_prefill_host_entry_point(B, mode, name, batch):
 def test_prefill_host_groups_long_items(B, mode):
     """Long items (65536 causal tokens, 8 chunks of 8192, 16/1 heads): the
     host-buffer call works through consecutive groups of Q pieces ({0},
-    {1..3}, {4, 5}, {6, 7}) so that copies overlap the work -- Pass-KV as four
-    on-chip launches, Pass-Q as the ring's pairs grouped by Q piece with each
-    group's merge before the next group's pairs -- and gives the device
+    {1, 2}, {3, 4}, {5, 6}, {7}) so that copies overlap the work -- Pass-KV as
+    five on-chip launches, Pass-Q as the ring's pairs grouped by Q piece with
+    each group's merge before the next group's pairs -- and gives the device
     call's result bit for bit."""
     g = torch.Generator(device="cuda")
     g.manual_seed(65536)
@@ -132,12 +132,12 @@ def test_prefill_host_groups_long_items(B, mode):
     kinds = [r[0] for r in recs if r[0] != "table"]
     if mode == B.PASS_KV:
         assert B.launch_mode(q, k, n, mode) == B.LAUNCH_SINGLE_ONCHIP
-        assert kinds == ["attn_tc_onchip"] * 4
+        assert kinds == ["attn_tc_onchip"] * 5
     else:
         assert B.launch_mode(q, k, n, mode) == B.LAUNCH_PER_STEP
-        # four groups, each: its pairs, then the merge of its pieces (piece 0
+        # five groups, each: its pairs, then the merge of its pieces (piece 0
         # has one pair, stored directly)
-        assert kinds == ["attn_tc"] + ["attn_tc", "mergeN"] * 3
+        assert kinds == ["attn_tc"] + ["attn_tc", "mergeN"] * 4
     assert torch.equal(oh, o_ref) and torch.equal(lh, l_ref)
 
 
